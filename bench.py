@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the librcc hot path on one GB300 (or N independent replicas).
+
+Workload: 8 logical ranks x 2^24 fp32 elements per rank (64 MiB each),
+gradient-like values N(0, 1e-2) with 0.1% of elements scaled x100, drawn on
+the device from fixed seeds.  One step is one pass of the whole hot path over
+that batch:
+  all_reduce sum, all_reduce mean, all_reduce max   (deterministic rank order)
+  reduce (sum) to root 7, broadcast from root 0
+  reduce_scatter (sum, shard 2^21), all_gather of those shards
+  grad_sync_adamw: the 8 rank buffers as the gradients of one 2^24-element
+    parameter tensor -> mean, unscale, fan-in-1024 statistics, 12-byte report,
+    clip, AdamW update (one fp32 state copy)
+Metric: algorithm GB/s = sum over the step's rows of R*N*bytes / step time.
+Every input (512 MiB per row) exceeds the 129 MB L2, so no flush is needed.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch under torchrun: each rank runs the same workload on its own
+GPU (replicas; no data-path collective); the timed region is bracketed by
+barriers and the max over ranks is reported.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+R = 8
+N = 1 << 24
+ES = 4
+ALG_BYTES_ROW = R * N * ES                     # R * N * s, one collective row
+ROWS = ["all_reduce_sum", "all_reduce_mean", "all_reduce_max", "reduce", "broadcast",
+        "reduce_scatter", "all_gather", "grad_sync_adamw"]
+# minimum HBM traffic of each row (bytes)
+MIN_TRAFFIC = {
+    "all_reduce_sum": 2 * R * N * ES, "all_reduce_mean": 2 * R * N * ES,
+    "all_reduce_max": 2 * R * N * ES,
+    "reduce": (R + 1) * N * ES, "broadcast": (1 + R) * N * ES,
+    "reduce_scatter": R * N * ES + N * ES, "all_gather": N * ES + R * N * ES,
+    # stats pass: R reads + mean-grad write; update: mean-grad read + p, m, v read+write
+    "grad_sync_adamw": (R * ES + ES) * N + (ES + 24) * N,
+}
+METRIC = "all_reduce algorithm GB/s and % of GB300 HBM roofline vs R, N, dtype (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "8 ranks x 2^24 fp32 per rank, gradient-like N(0,1e-2) + 0.1% x100"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def combine_ranks(local_ms, local_units, world, device="cpu"):
+    """Max of the per-rank times and sum of the per-rank work over the group."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ environment facts
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in d and isinstance(d[key], (int, float)):
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("collectives.cuh", "collectives_f32.cu"):
+        with open(os.path.join(ROOT, "gradient_sync_rcc_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the all_reduce kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "all_reduce_f32_8x2p24_ncu.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel-source-sha256-16:\s*([0-9a-f]+)", text)
+    tb = re.search(r"traffic-bytes-per-launch:\s*([0-9]+)", text)
+    if not sha or not tb or sha.group(1) != kernel_source_sha():
+        return None
+    return int(tb.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Workload:
+    def __init__(self, device):
+        import torch
+        from gradient_sync_rcc_gb300 import rcc, synth
+        self.torch, self.rcc = torch, rcc
+        self.dev = device
+        self.ins = synth.gpu_rank_buffers("grad", R, N, torch.float32, (2, 1), device)
+        self.ar = [torch.empty(N, device=device) for _ in range(R)]
+        self.red = torch.empty(N, device=device)
+        self.bc = [torch.empty(N, device=device) for _ in range(R)]
+        self.rs = [torch.empty(N // R, device=device) for _ in range(R)]
+        self.ag = [torch.empty(N, device=device) for _ in range(R)]
+        p0 = synth.gpu_draw("normal:0.02", N, torch.float32, (2, 2), device)
+        self.gs_tensors = [dict(grads=self.ins, params=[p0], exp_avg=[torch.zeros(N, device=device)],
+                                exp_avg_sq=[torch.zeros(N, device=device)],
+                                mean_grad=torch.empty(N, device=device))]
+        self.sets = rcc.ParamSets(self.gs_tensors)
+        self.cfg = rcc.adamw_cfg(replicas=1, max_grad_norm=1.0)
+        self.state = rcc.optim_state(scale=1.0)
+
+    def step(self, h, events=None):
+        rcc = self.rcc
+
+        def mark(i):
+            if events is not None:
+                events[i].record()
+
+        mark(0)
+        rcc.all_reduce(h, self.ins, self.ar, "sum")
+        mark(1)
+        rcc.all_reduce(h, self.ins, self.ar, "mean")
+        mark(2)
+        rcc.all_reduce(h, self.ins, self.ar, "max")
+        mark(3)
+        rcc.reduce(h, self.ins, self.red, root=R - 1, op="sum")
+        mark(4)
+        rcc.broadcast(h, self.ins[0], self.bc, root=0)
+        mark(5)
+        rcc.reduce_scatter(h, self.ins, self.rs, "sum")
+        mark(6)
+        rcc.all_gather(h, self.rs, self.ag)
+        mark(7)
+        rep = rcc.grad_sync_adamw(h, self.sets, self.cfg, self.state)
+        mark(8)
+        return rep
+
+
+def copy_bandwidth(torch, device):
+    """D2D copy of 2 GiB (read + write counted), for context only."""
+    a = torch.empty(1 << 29, dtype=torch.float32, device=device)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        b.copy_(a)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(10):
+        b.copy_(a)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / 10
+    del a, b
+    return 2 * (1 << 31) / (ms * 1e-3) / 1e9
+
+
+def bench_ours(args):
+    import torch
+    from gradient_sync_rcc_gb300 import build, rcc
+    rank, world, local = dist_env()
+    build.build()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    device = "cuda:%d" % local
+    wl = Workload(device)
+    h = rcc.register(local, R, rcc.F32, True)
+    try:
+        for _ in range(max(args.warmup, 3)):
+            wl.step(h)
+        torch.cuda.synchronize()
+        K = args.steps
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
+              for _ in range(K)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.4)                 # let the sampler see the load from the first steps
+        launches0 = rcc.launch_count()
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(K):
+            wl.step(h, ev[k])
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        launches = rcc.launch_count() - launches0
+        clocks = sampler.stop()
+        ms_total = start.elapsed_time(end)
+        row_ms = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+                  for i, name in enumerate(ROWS)}
+
+        # end to end: inputs from pinned host memory, result read back, every step
+        Ke = max(3, min(K, 20))
+        host_in = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(R)]
+        for x, d in zip(host_in, wl.ins):
+            x.copy_(d)
+        host_out = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(Ke):
+            for x, d in zip(host_in, wl.ins):
+                d.copy_(x, non_blocking=True)
+            wl.step(h)
+            host_out.copy_(wl.ar[0], non_blocking=True)
+            torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
+        barrier(world)
+        copy_gbs = copy_bandwidth(torch, device)
+    finally:
+        rcc.finish(h)
+
+    ms_step = ms_total / K
+    alg_step = ALG_BYTES_ROW * len(ROWS)
+    max_ms, total_units = combine_ranks(ms_step, alg_step, world, device)
+    max_e2e, total_e2e = combine_ranks(e2e_ms, alg_step, world, device)
+    if rank != 0:
+        return
+    peak, peak_src = peak_hbm()
+    ar_ms = statistics.mean([row_ms["all_reduce_sum"], row_ms["all_reduce_mean"],
+                             row_ms["all_reduce_max"]])
+    ar_traffic = MIN_TRAFFIC["all_reduce_sum"]
+    achieved = ar_traffic / (ar_ms * 1e-3) / 1e9
+    rows = {}
+    for name in ROWS:
+        t = row_ms[name]
+        gbs = MIN_TRAFFIC[name] / (t * 1e-3) / 1e9
+        rows[name] = {"ms": round(t, 4), "algbw_gbs": round(ALG_BYTES_ROW / (t * 1e-3) / 1e9, 1),
+                      "traffic_gbs": round(gbs, 1), "frac_of_" + peak_src: round(gbs / peak, 4)}
+    out = {
+        "metric": METRIC,
+        "value": round(total_units / (max_ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(max_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded device draws)",
+        "config": {"workload": WORKLOAD, "ranks": R, "elements_per_rank": N,
+                   "rows_per_step": ROWS, "mode": "deterministic rank order",
+                   "adamw_replicas": 1, "l2": "inputs 512 MiB per row > 129 MB L2, no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "all_reduce (multi-pointer pass, fp32, R=8, N=2^24)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
+                     "algorithmic_bytes_per_launch": ar_traffic,
+                     "avg_launch_ms": round(ar_ms, 4)},
+        "rows": rows,
+        "e2e": {"value": round(total_e2e / (max_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(max_e2e, 3),
+                "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES + 12},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "d2d_copy_gbs_measured_here": round(copy_gbs, 1),
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(target_s=10.0)
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ the oracle on host cores
+
+def oracle_step(orc, xs, state):
+    """One pass of the step's rows over host arrays, in the oracle."""
+    n = xs[0].size
+    for op in ("sum", "mean", "max"):
+        orc.all_reduce(xs, op)
+    out = np.empty(n, np.float32)
+    orc.reduce(xs, "sum", out)
+    orc.broadcast(xs[0], [np.empty(n, np.float32) for _ in range(len(xs))])
+    rs = orc.reduce_scatter(xs, "sum")
+    orc.all_gather(rs)
+    p, m, v, sc, t = state
+    t, _, _ = orc.grad_sync_adamw_step([xs], [p], [m], [v], lr=1e-3, beta1=0.9, beta2=0.999,
+                                       eps=1e-8, weight_decay=0.01, max_grad_norm=1.0, step=t,
+                                       scaler=sc)
+    state[4] = t
+
+
+def _oracle_setup(n):
+    import oracle as orc
+    from gradient_sync_rcc_gb300 import synth
+    orc.build.build()
+    xs = synth.rank_buffers("grad", R, n, 2, 3)
+    p = synth.normal(n, 0.02, 2, 4)
+    state = [p, np.zeros(n, np.float32), np.zeros(n, np.float32), orc.scaler_new(1.0), 0]
+    return orc, xs, state
+
+
+def cpu_baseline(target_s=10.0, n=1 << 22):
+    orc, xs, state = _oracle_setup(n)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(orc, xs, state)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    alg = R * n * ES * len(ROWS) * reps
+    return {"value": round(alg / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "the step's 8 rows over 8 ranks x 2^22 fp32 (1/4 of the workload), "
+                      "%d passes, %.1f s single-threaded" % (reps, el)}
+
+
+def bench_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    n = 1 << 20
+    orc, xs, state = _oracle_setup(n)
+    for _ in range(max(args.warmup, 3)):
+        oracle_step(orc, xs, state)
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_step(orc, xs, state)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / K
+    value = R * n * ES * len(ROWS) / (ms * 1e-3) / 1e9
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+           "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
+           "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded host draws)",
+           "config": {"workload": WORKLOAD, "ranks": R, "elements_per_rank": N,
+                      "rows_per_step": ROWS, "mode": "deterministic rank order"},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                            "kind": "oracle",
+                            "sample": "each step: the 8 rows over 8 ranks x 2^20 fp32 "
+                                      "(1/16 of the workload), single-threaded"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

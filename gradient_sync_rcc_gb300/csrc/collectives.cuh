@@ -1,0 +1,402 @@
+// collectives.cuh -- the multi-pointer pass behind every librcc collective.
+//
+// Replaces the ring schedule with host-staged transfers that the ruCCL README
+// describes (§5 "CUDA example", §6 data path) by a single pass over HBM: all R
+// rank buffers live on one GPU, so each output element is produced by one
+// thread that loads the element from every source rank (16-byte vectors,
+// coalesced, L1-bypassing streaming loads) and stores the result to every
+// destination (streaming stores).  Minimum traffic, no staging, no exchange.
+//
+// Arithmetic is fp32 for both element types (bf16 is widened exactly and the
+// result is rounded once to nearest-even).  Sums fold ranks in the order
+// 0..R-1 (deterministic mode) or in a pairwise tree (fast mode); mean divides
+// the sum by R with an IEEE division; max/min keep the lowest rank among
+// equals and turn any NaN into the quiet NaN 0x7FC00000.
+//
+// Included by collectives_f32.cu and collectives_bf16.cu, one element type each.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "rcc_internal.h"
+
+namespace rcc {
+namespace mp {
+
+constexpr uint32_t kCanonicalNaN = 0x7FC00000u;
+
+// ---- memory access -------------------------------------------------------
+// Streaming 16-byte load through the non-coherent path without L1
+// allocation: every input element is read exactly once.  Volatile keeps the
+// loads and stores of one thread in program order (in-place all_reduce reads
+// an element before the same thread overwrites it).
+__device__ __forceinline__ uint4 ld_vec(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Streaming (evict-first) 16-byte store: outputs are not re-read by this pass.
+__device__ __forceinline__ void st_vec(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---- element types ---------------------------------------------------------
+
+// fp32 -> bf16 bits, round to nearest even (hardware cvt); a NaN keeps its
+// sign and high payload bits and is made quiet, the same rule for every op.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  if (lo != lo) r = (r & 0xFFFF0000u) | ((__float_as_uint(lo) >> 16) | 0x40u);
+  if (hi != hi) r = (r & 0x0000FFFFu) | ((((__float_as_uint(hi) >> 16) | 0x40u)) << 16);
+  return r;
+}
+
+__device__ __forceinline__ uint16_t bf16_rn(float f) {
+  return (uint16_t)(bf16x2_rn(f, 0.0f) & 0xFFFFu);
+}
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int kPerVec = 4;
+  static constexpr int kBytes = 4;
+  __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+  __device__ static __forceinline__ float load(const void* p, size_t i) {
+    return static_cast<const float*>(p)[i];
+  }
+  __device__ static __forceinline__ void store(void* p, size_t i, float f) {
+    static_cast<float*>(p)[i] = f;
+  }
+  __device__ static __forceinline__ void copy(const void* s, void* d, size_t i) {
+    static_cast<uint32_t*>(d)[i] = static_cast<const uint32_t*>(s)[i];
+  }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kPerVec = 8;
+  static constexpr int kBytes = 2;
+  __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(bf16x2_rn(f[0], f[1]), bf16x2_rn(f[2], f[3]),
+                      bf16x2_rn(f[4], f[5]), bf16x2_rn(f[6], f[7]));
+  }
+  __device__ static __forceinline__ float load(const void* p, size_t i) {
+    return __uint_as_float((uint32_t)static_cast<const uint16_t*>(p)[i] << 16);
+  }
+  __device__ static __forceinline__ void store(void* p, size_t i, float f) {
+    static_cast<uint16_t*>(p)[i] = bf16_rn(f);
+  }
+  __device__ static __forceinline__ void copy(const void* s, void* d, size_t i) {
+    static_cast<uint16_t*>(d)[i] = static_cast<const uint16_t*>(s)[i];
+  }
+};
+
+// ---- reductions over ranks ---------------------------------------------------
+
+__host__ __device__ constexpr int pow2_below(int n) {
+  int p = 1;
+  while (p * 2 < n) p *= 2;
+  return p;
+}
+
+// Pairwise tree over x[LO, HI): split at the largest power of two below the
+// length, e.g. 5 ranks -> ((x0+x1)+(x2+x3))+x4.
+template <int LO, int HI>
+struct Tree {
+  __device__ static __forceinline__ float sum(const float* x) {
+    if constexpr (HI - LO == 1) {
+      return x[LO];
+    } else {
+      constexpr int mid = LO + pow2_below(HI - LO);
+      return __fadd_rn(Tree<LO, mid>::sum(x), Tree<mid, HI>::sum(x));
+    }
+  }
+};
+
+// Running state of one output lane.  Used in rank order: init(x_0), then
+// add(x_1), ..., add(x_{R-1}).
+template <int RED>
+struct Acc {
+  float v;
+  bool nan;
+  __device__ __forceinline__ void init(float x) {
+    v = x;
+    nan = (x != x);
+  }
+  __device__ __forceinline__ void add(float x) {
+    if constexpr (RED == kRedSum) {
+      v = __fadd_rn(v, x);
+    } else {
+      nan |= (x != x);
+      if (RED == kRedMax ? (x > v) : (x < v)) v = x;
+    }
+  }
+  __device__ __forceinline__ float result(int mean_div) const {
+    if constexpr (RED == kRedSum) {
+      return mean_div > 0 ? __fdiv_rn(v, (float)mean_div) : v;
+    } else {
+      return nan ? __uint_as_float(kCanonicalNaN) : v;
+    }
+  }
+};
+
+template <int NS, int RED, bool FAST>
+__device__ __forceinline__ float reduce_lane(const float (&x)[NS], int mean_div) {
+  if constexpr (RED == kRedSum && FAST) {
+    float s = Tree<0, NS>::sum(x);
+    return mean_div > 0 ? __fdiv_rn(s, (float)mean_div) : s;
+  } else {
+    Acc<RED> a;
+    a.init(x[0]);
+#pragma unroll
+    for (int q = 1; q < NS; ++q) a.add(x[q]);
+    return a.result(mean_div);
+  }
+}
+
+// ---- the pass ----------------------------------------------------------------
+
+// Per-segment views of the argument block.
+struct SegView {
+  const MultiPtrArgs& a;
+  int seg;
+  size_t soff, doff;  // element offsets of this segment
+  __device__ __forceinline__ const void* src(int q, int eb) const {
+    const void* base = a.src_per_seg ? a.src[seg] : a.src[q];
+    return static_cast<const char*>(base) + soff * eb;
+  }
+  __device__ __forceinline__ void* dst(int d, int eb) const {
+    void* base = a.dst_per_seg ? a.dst[seg] : a.dst[d];
+    return static_cast<char*>(base) + doff * eb;
+  }
+  __device__ __forceinline__ int ndst() const { return a.dst_per_seg ? 1 : a.ndst; }
+};
+
+// NS > 0: compile-time number of sources (U vectors per thread in flight per
+// source); NS == 0: runtime count (any R up to kMaxRanks), sources loaded in
+// groups of 8 and folded in rank order.
+template <typename T, int NS, int RED, bool FAST, int U>
+__global__ void __launch_bounds__(kThreads)
+    mp_kernel(const __grid_constant__ MultiPtrArgs a) {
+  using E = Elem<T>;
+  constexpr int EPV = E::kPerVec;
+  constexpr int EB = E::kBytes;
+  const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
+                   (size_t)blockIdx.y * a.dst_seg_stride};
+  const int ndst = sv.ndst();
+  const size_t nv = a.vec_ok ? a.n / EPV : 0;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+
+  if constexpr (NS > 0) {
+    const char* sp[NS];
+#pragma unroll
+    for (int q = 0; q < NS; ++q) sp[q] = static_cast<const char*>(sv.src(q, EB));
+
+    for (size_t base = (size_t)blockIdx.x * blockDim.x * U + threadIdx.x; base < nv;
+         base += nthreads * U) {
+      uint4 v[U][NS];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t idx = base + (size_t)u * blockDim.x;
+        if (idx < nv) {
+#pragma unroll
+          for (int q = 0; q < NS; ++q) v[u][q] = ld_vec(sp[q] + idx * 16);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t idx = base + (size_t)u * blockDim.x;
+        if (idx < nv) {
+          uint4 out;
+          if constexpr (RED == kRedCopy) {
+            out = v[u][0];
+          } else {
+            float f[NS][EPV];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) E::unpack(v[u][q], f[q]);
+            float r[EPV];
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              float x[NS];
+#pragma unroll
+              for (int q = 0; q < NS; ++q) x[q] = f[q][e];
+              r[e] = reduce_lane<NS, RED, FAST>(x, a.mean_div);
+            }
+            out = E::pack(r);
+          }
+          for (int d = 0; d < ndst; ++d)
+            st_vec(static_cast<char*>(sv.dst(d, EB)) + idx * 16, out);
+        }
+      }
+    }
+  } else {
+    // runtime rank count: rank order fold in groups of 8 sources
+    const int R = a.nsrc;
+    for (size_t idx = tid; idx < nv; idx += nthreads) {
+      Acc<RED> acc[EPV];
+      for (int q0 = 0; q0 < R; q0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (q0 + k < R) v[k] = ld_vec(static_cast<const char*>(sv.src(q0 + k, EB)) + idx * 16);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (q0 + k < R) {
+            float f[EPV];
+            E::unpack(v[k], f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              if (q0 + k == 0)
+                acc[e].init(f[e]);
+              else
+                acc[e].add(f[e]);
+            }
+          }
+        }
+      }
+      float r[EPV];
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) r[e] = acc[e].result(a.mean_div);
+      const uint4 out = E::pack(r);
+      for (int d = 0; d < ndst; ++d)
+        st_vec(static_cast<char*>(sv.dst(d, EB)) + idx * 16, out);
+    }
+  }
+
+  // scalar elements: the ragged tail after the vectors, or everything when
+  // some address is not 16-byte aligned
+  for (size_t i = nv * EPV + tid; i < a.n; i += nthreads) {
+    if constexpr (RED == kRedCopy) {
+      const void* s = sv.src(0, EB);
+      for (int d = 0; d < ndst; ++d) E::copy(s, sv.dst(d, EB), i);
+    } else if constexpr (NS > 0) {
+      float x[NS];
+#pragma unroll
+      for (int q = 0; q < NS; ++q) x[q] = E::load(sv.src(q, EB), i);
+      const float y = reduce_lane<NS, RED, FAST>(x, a.mean_div);
+      for (int d = 0; d < ndst; ++d) E::store(sv.dst(d, EB), i, y);
+    } else {
+      Acc<RED> acc;
+      acc.init(E::load(sv.src(0, EB), i));
+      for (int q = 1; q < a.nsrc; ++q) acc.add(E::load(sv.src(q, EB), i));
+      const float y = acc.result(a.mean_div);
+      for (int d = 0; d < ndst; ++d) E::store(sv.dst(d, EB), i, y);
+    }
+  }
+}
+
+// ---- host-side dispatch -------------------------------------------------------
+
+// Vectors per thread in flight for each source count: enough 16-byte loads
+// outstanding per thread (U * NS >= 4..8) to cover HBM latency.
+constexpr int unroll_for(int ns, int red) {
+  return red == kRedCopy ? 4 : ns <= 2 ? 4 : ns <= 4 ? 2 : 1;
+}
+
+inline int sm_count() {
+  static int cached = -1;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int cached_dev = -1;
+  if (cached < 0 || cached_dev != dev) {
+    cudaDeviceGetAttribute(&cached, cudaDevAttrMultiProcessorCount, dev);
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+inline int resident_blocks(const void* fn) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(fn);
+  if (it != cache.end()) return it->second;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
+  if (per_sm < 1) per_sm = 1;
+  cache[fn] = per_sm;
+  return per_sm;
+}
+
+template <typename T, int NS, int RED, bool FAST>
+cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+  constexpr int U = NS > 0 ? unroll_for(NS, RED) : 1;
+  constexpr int EPV = Elem<T>::kPerVec;
+  auto fn = mp_kernel<T, NS, RED, FAST, U>;
+  const size_t nv = a.vec_ok ? a.n / EPV : 0;
+  const size_t tail = a.n - nv * EPV;
+  size_t want = (nv + (size_t)kThreads * U - 1) / ((size_t)kThreads * U);
+  const size_t want_tail = (tail + kThreads - 1) / kThreads;
+  if (want_tail > want) want = want_tail;
+  if (want < 1) want = 1;
+  // one full wave of resident blocks across all segments, sized on the SM count
+  size_t cap = (size_t)resident_blocks((const void*)fn) * sm_count() / (size_t)nseg;
+  if (cap < 1) cap = 1;
+  const unsigned gx = (unsigned)(want < cap ? want : cap);
+  fn<<<dim3(gx, (unsigned)nseg), kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, int RED, bool FAST>
+cudaError_t launch_red(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+  const int ns = a.src_per_seg ? 1 : a.nsrc;
+  switch (ns) {
+    case 1: return launch_ns<T, 1, RED, false>(nseg, a, stream);
+    case 2: return launch_ns<T, 2, RED, false>(nseg, a, stream);
+    case 3: return launch_ns<T, 3, RED, false>(nseg, a, stream);
+    case 4: return launch_ns<T, 4, RED, FAST>(nseg, a, stream);
+    case 5: return launch_ns<T, 5, RED, FAST>(nseg, a, stream);
+    case 6: return launch_ns<T, 6, RED, FAST>(nseg, a, stream);
+    case 7: return launch_ns<T, 7, RED, FAST>(nseg, a, stream);
+    case 8: return launch_ns<T, 8, RED, FAST>(nseg, a, stream);
+    default: return launch_ns<T, 0, RED, false>(nseg, a, stream);
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(Red red, bool fast, int nseg, const MultiPtrArgs& a,
+                         cudaStream_t stream) {
+  switch (red) {
+    case kRedSum:
+      return fast ? launch_red<T, kRedSum, true>(nseg, a, stream)
+                  : launch_red<T, kRedSum, false>(nseg, a, stream);
+    case kRedMax: return launch_red<T, kRedMax, false>(nseg, a, stream);
+    case kRedMin: return launch_red<T, kRedMin, false>(nseg, a, stream);
+    case kRedCopy: return launch_ns<T, 1, kRedCopy, false>(nseg, a, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mp
+}  // namespace rcc

@@ -1,0 +1,9 @@
+// collectives_f32.cu -- fp32 instantiations of the multi-pointer pass.
+#include "collectives.cuh"
+
+namespace rcc {
+cudaError_t launch_multi_ptr_f32(Red red, bool fast, int nseg, const MultiPtrArgs& a,
+                                 cudaStream_t stream) {
+  return mp::launch_typed<float>(red, fast, nseg, a, stream);
+}
+}  // namespace rcc

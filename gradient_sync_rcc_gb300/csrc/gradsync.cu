@@ -1,0 +1,372 @@
+// gradsync.cu -- the gradient-sync + fused AdamW kernel chain.
+//
+// [ruCCL README §6 "Collective training"]: gradients are all-reduced with
+// ReduceOperation::Mean, then handed to the optimizer step.
+// [RUDA docs "Training and saving state", section "Native PyTorch training on
+// ruda:0"]: ruda_torch.AdamW(fused_step, max_grad_norm, hierarchical_stats)
+// does a read-only gradient analysis, global L2 clipping after unscale, and
+// hierarchical statistics (fan-in 1024, at most two extra combine kernels, a
+// reused reduction region of at most 49,200 bytes, none for <= 1024 rows);
+// a 12-byte report is read back before the update; a non-finite gradient
+// skips the whole step; master weights and moments are FP32; the update is one
+// kernel per parameter, not one kernel for the whole model.
+//
+// Kernels:
+//   gs_stats_kernel   all_reduce Mean of the R scaled gradients + unscale,
+//                     optional store of the mean gradient, and one 12-byte row
+//                     {sum g^2 (fp64), non-finite count (u32)} per block
+//   gs_combine_kernel one fan-in-1024 combine level: 1024 rows -> 1 row
+//   gs_report_kernel  the last <= 1024 rows (or all rows, flat) -> report
+//   gs_update_kernel  one launch per tensor: clip, decoupled decay, moments,
+//                     bias-corrected step on every optimizer-state replica
+//
+// Row layout: three u32 words {low, high word of the fp64 sum, count}.
+#include <cuda_runtime.h>
+
+#include "rcc_internal.h"
+
+namespace rcc {
+namespace gs {
+
+constexpr int kFanIn = 1024;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint4 ld_vec(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Plain (write-back) 16-byte load for state that this kernel also writes.
+__device__ __forceinline__ float4 ld_state(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+__device__ __forceinline__ void st_vec(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---- per-thread sum of squares -------------------------------------------
+// The squares are summed in a pair of fp32 words (value + running error) with
+// error-free transformations: the product error fmaf(g, g, -g*g) is exact and
+// TwoSum keeps the addition error, so a thread's partial is good to ~2^-44
+// relative before it is widened to fp64 -- without spending GB300's scarce
+// fp64 issue slots on every element.  Magnitudes outside [2^-40, 2^40] (where
+// the error terms could underflow or the pair could overflow) go straight to
+// an fp64 accumulator.  Non-finite values are counted and not summed.
+struct SqAcc {
+  float hi = 0.0f, lo = 0.0f;
+  double wide = 0.0;
+  uint32_t nonfinite = 0;
+  __device__ __forceinline__ void add(float g) {
+    const float a = fabsf(g);
+    if (a <= 0x1p40f && a >= 0x1p-40f) {
+      const float p = __fmul_rn(g, g);
+      const float pe = __fmaf_rn(g, g, -p);
+      const float t = __fadd_rn(hi, p);
+      const float bp = __fsub_rn(t, hi);
+      const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+      hi = t;
+      lo = __fadd_rn(lo, __fadd_rn(err, pe));
+    } else if (!(a <= 3.402823466e38f)) {  // Inf or NaN
+      nonfinite += 1;
+    } else if (a != 0.0f) {
+      wide += (double)g * (double)g;
+    }
+  }
+  __device__ __forceinline__ double value() const {
+    return (double)hi + (double)lo + wide;
+  }
+};
+
+__device__ __forceinline__ void block_reduce_row(double s, uint32_t c, uint32_t* row) {
+  __shared__ double ws[kWarps];
+  __shared__ uint32_t wc[kWarps];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, off);
+  c = __reduce_add_sync(0xFFFFFFFFu, c);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    ws[warp] = s;
+    wc[warp] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    s = lane < kWarps ? ws[lane] : 0.0;
+    c = lane < kWarps ? wc[lane] : 0u;
+#pragma unroll
+    for (int off = kWarps / 2; off > 0; off >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, off);
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (lane == 0) {
+      const unsigned long long u = (unsigned long long)__double_as_longlong(s);
+      row[0] = (uint32_t)(u & 0xFFFFFFFFull);
+      row[1] = (uint32_t)(u >> 32);
+      row[2] = c;
+    }
+  }
+}
+
+// mean of R scaled gradients in rank order, then unscale: both steps fp32 IEEE
+__device__ __forceinline__ float mean_unscale(const float* x, int R, float inv_scale) {
+  float s = x[0];
+  for (int q = 1; q < R; ++q) s = __fadd_rn(s, x[q]);
+  return __fmul_rn(__fdiv_rn(s, (float)R), inv_scale);
+}
+
+template <int RC>  // RC > 0: compile-time rank count; 0: runtime (a.R)
+__global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constant__ GsStatsArgs a) {
+  const uint64_t row = blockIdx.x;
+  // the tensor owning this row: last t with row_begin <= row
+  uint32_t lo = 0, hi = a.num_tensors - 1;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi + 1) >> 1;
+    if (a.tensors[mid].row_begin <= row)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const GsTensor t = a.tensors[lo];
+  const int R = RC > 0 ? RC : a.R;
+  const float* const* g = a.grads + t.grad_slot;
+  const uint64_t c0 = (row - t.row_begin) * (uint64_t)a.elems_per_row;
+  uint64_t c1 = c0 + a.elems_per_row;
+  if (c1 > t.numel) c1 = t.numel;
+
+  SqAcc acc;
+  uint64_t scalar_from = c0;
+  if (t.vec_ok) {
+    // c0 is a multiple of 4 (elems_per_row is), so vectors start aligned
+    const uint64_t v0 = c0 / 4, v1 = c1 / 4;
+    scalar_from = v1 * 4;
+    for (uint64_t v = v0 + threadIdx.x; v < v1; v += 2 * kThreads) {
+      uint4 x[2][RC > 0 ? RC : 1];
+      if constexpr (RC > 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint64_t vi = v + (uint64_t)u * kThreads;
+          if (vi < v1) {
+#pragma unroll
+            for (int q = 0; q < RC; ++q) x[u][q] = ld_vec(g[q] + vi * 4);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint64_t vi = v + (uint64_t)u * kThreads;
+        if (vi >= v1) continue;
+        float m[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (RC > 0) {
+            float col[RC];
+#pragma unroll
+            for (int q = 0; q < RC; ++q)
+              col[q] = __uint_as_float(e == 0 ? x[u][q].x : e == 1 ? x[u][q].y
+                                        : e == 2 ? x[u][q].z : x[u][q].w);
+            m[e] = mean_unscale(col, RC, a.inv_scale);
+          } else {
+            float s = g[0][vi * 4 + e];
+            for (int q = 1; q < R; ++q) s = __fadd_rn(s, g[q][vi * 4 + e]);
+            m[e] = __fmul_rn(__fdiv_rn(s, (float)R), a.inv_scale);
+          }
+          acc.add(m[e]);
+        }
+        if (t.mean_grad)
+          st_vec(t.mean_grad + vi * 4, make_uint4(__float_as_uint(m[0]), __float_as_uint(m[1]),
+                                                  __float_as_uint(m[2]), __float_as_uint(m[3])));
+      }
+    }
+  }
+  for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads) {
+    float s = g[0][i];
+    for (int q = 1; q < R; ++q) s = __fadd_rn(s, g[q][i]);
+    const float m = __fmul_rn(__fdiv_rn(s, (float)R), a.inv_scale);
+    acc.add(m);
+    if (t.mean_grad) t.mean_grad[i] = m;
+  }
+  block_reduce_row(acc.value(), acc.nonfinite, a.rows + row * 3);
+}
+
+__device__ __forceinline__ double row_sum(const uint32_t* r) {
+  return __longlong_as_double((long long)(((unsigned long long)r[1] << 32) | r[0]));
+}
+
+// one combine level: block b reduces rows [b*1024, min((b+1)*1024, nrows))
+__global__ void __launch_bounds__(kThreads)
+    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out) {
+  const uint64_t r0 = (uint64_t)blockIdx.x * kFanIn;
+  double s = 0.0;
+  uint32_t c = 0;
+#pragma unroll
+  for (int k = 0; k < kFanIn / kThreads; ++k) {
+    const uint64_t r = r0 + threadIdx.x + (uint64_t)k * kThreads;
+    if (r < nrows) {
+      s += row_sum(in + r * 3);
+      c += in[r * 3 + 2];
+    }
+  }
+  block_reduce_row(s, c, out + (uint64_t)blockIdx.x * 3);
+}
+
+// the final reduction into the 12-byte report (one block, any row count)
+__global__ void __launch_bounds__(kThreads)
+    gs_report_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ report) {
+  double s = 0.0;
+  uint32_t c = 0;
+  for (uint64_t r = threadIdx.x; r < nrows; r += kThreads) {
+    s += row_sum(in + r * 3);
+    c += in[r * 3 + 2];
+  }
+  block_reduce_row(s, c, report);
+}
+
+// ---- AdamW update ---------------------------------------------------------
+// Element arithmetic, each operation rounded once (no contraction):
+//   g' = g*coef; p = p*decay; m = b1*m + (1-b1)*g'; v = b2*v + (1-b2)*(g'*g');
+//   p = p - step_size * (m / (sqrt(v)*inv_bc2_sqrt + eps))
+__device__ __forceinline__ void adamw_elem(float g, const AdamWScalars& s, float& p,
+                                           float& m, float& v) {
+  const float pd = __fmul_rn(p, s.decay);
+  const float mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.one_minus_beta1, g));
+  const float vi = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.one_minus_beta2, __fmul_rn(g, g)));
+  const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vi), s.inv_bc2_sqrt), s.eps);
+  p = __fsub_rn(pd, __fmul_rn(s.step_size, __fdiv_rn(mi, denom)));
+  m = mi;
+  v = vi;
+}
+
+// ptr table layout of one tensor: params[0..rep), exp_avg[0..rep), exp_avg_sq[0..rep)
+template <int REP>  // REP > 0: compile-time replica count; 0: runtime
+__global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
+  const int rep = REP > 0 ? REP : a.replicas;
+  float* const* P = a.state;
+  const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
+  const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+  const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
+  for (uint64_t v = tid; v < nv; v += nthreads) {
+    float gv[4];
+    if (a.mean_grad) {
+      const uint4 x = ld_vec(a.mean_grad + v * 4);
+      gv[0] = __uint_as_float(x.x);
+      gv[1] = __uint_as_float(x.y);
+      gv[2] = __uint_as_float(x.z);
+      gv[3] = __uint_as_float(x.w);
+    } else {
+      float4 acc = *reinterpret_cast<const float4*>(a.grads[0] + v * 4);
+      for (int q = 1; q < a.R; ++q) {
+        const float4 y = *reinterpret_cast<const float4*>(a.grads[q] + v * 4);
+        acc.x = __fadd_rn(acc.x, y.x);
+        acc.y = __fadd_rn(acc.y, y.y);
+        acc.z = __fadd_rn(acc.z, y.z);
+        acc.w = __fadd_rn(acc.w, y.w);
+      }
+      const float Rf = (float)a.R;
+      gv[0] = __fmul_rn(__fdiv_rn(acc.x, Rf), a.inv_scale);
+      gv[1] = __fmul_rn(__fdiv_rn(acc.y, Rf), a.inv_scale);
+      gv[2] = __fmul_rn(__fdiv_rn(acc.z, Rf), a.inv_scale);
+      gv[3] = __fmul_rn(__fdiv_rn(acc.w, Rf), a.inv_scale);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], a.clip_coef);
+    constexpr int RB = REP > 0 ? REP : 4;  // replicas per batch of loads
+    for (int r0 = 0; r0 < rep; r0 += RB) {
+      float4 p[RB], m[RB], w[RB];
+#pragma unroll
+      for (int k = 0; k < RB; ++k) {
+        if (r0 + k < rep) {
+          p[k] = ld_state(P[r0 + k] + v * 4);
+          m[k] = ld_state(P[rep + r0 + k] + v * 4);
+          w[k] = ld_state(P[2 * rep + r0 + k] + v * 4);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < RB; ++k) {
+        if (r0 + k < rep) {
+          adamw_elem(gv[0], a.s, p[k].x, m[k].x, w[k].x);
+          adamw_elem(gv[1], a.s, p[k].y, m[k].y, w[k].y);
+          adamw_elem(gv[2], a.s, p[k].z, m[k].z, w[k].z);
+          adamw_elem(gv[3], a.s, p[k].w, m[k].w, w[k].w);
+          *reinterpret_cast<float4*>(P[r0 + k] + v * 4) = p[k];
+          *reinterpret_cast<float4*>(P[rep + r0 + k] + v * 4) = m[k];
+          *reinterpret_cast<float4*>(P[2 * rep + r0 + k] + v * 4) = w[k];
+        }
+      }
+    }
+  }
+  for (uint64_t i = nv * 4 + tid; i < a.numel; i += nthreads) {
+    float g;
+    if (a.mean_grad) {
+      g = a.mean_grad[i];
+    } else {
+      float s = a.grads[0][i];
+      for (int q = 1; q < a.R; ++q) s = __fadd_rn(s, a.grads[q][i]);
+      g = __fmul_rn(__fdiv_rn(s, (float)a.R), a.inv_scale);
+    }
+    g = __fmul_rn(g, a.clip_coef);
+    for (int r = 0; r < rep; ++r) {
+      float p = P[r][i], m = P[rep + r][i], w = P[2 * rep + r][i];
+      adamw_elem(g, a.s, p, m, w);
+      P[r][i] = p;
+      P[rep + r][i] = m;
+      P[2 * rep + r][i] = w;
+    }
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace gs
+
+cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
+  if (a.total_rows == 0) return cudaSuccess;
+  const dim3 grid((unsigned)a.total_rows);
+  switch (a.R) {
+    case 1: gs::gs_stats_kernel<1><<<grid, kThreads, 0, stream>>>(a); break;
+    case 2: gs::gs_stats_kernel<2><<<grid, kThreads, 0, stream>>>(a); break;
+    case 4: gs::gs_stats_kernel<4><<<grid, kThreads, 0, stream>>>(a); break;
+    case 8: gs::gs_stats_kernel<8><<<grid, kThreads, 0, stream>>>(a); break;
+    default: gs::gs_stats_kernel<0><<<grid, kThreads, 0, stream>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
+                              cudaStream_t stream) {
+  const unsigned blocks = (unsigned)((nrows + gs::kFanIn - 1) / gs::kFanIn);
+  gs::gs_combine_kernel<<<blocks, kThreads, 0, stream>>>(in, nrows, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
+                             cudaStream_t stream) {
+  gs::gs_report_kernel<<<1, kThreads, 0, stream>>>(in, nrows, report);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
+  const uint64_t units = a.vec_ok ? (a.numel + 3) / 4 : a.numel;
+  uint64_t blocks = (units + kThreads - 1) / kThreads;
+  // grid-stride beyond a few full waves of the SMs
+  const uint64_t cap = (uint64_t)gs::sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  switch (a.replicas) {
+    case 1: gs::gs_update_kernel<1><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
+    case 2: gs::gs_update_kernel<2><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
+    case 4: gs::gs_update_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
+    case 8: gs::gs_update_kernel<8><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
+    default: gs::gs_update_kernel<0><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rcc

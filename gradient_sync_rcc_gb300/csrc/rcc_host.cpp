@@ -1,0 +1,860 @@
+// rcc_host.cpp -- librcc host layer: session registry, argument validation,
+// launch planning and the gradient-sync step driver.  Implements include/rcc.h.
+//
+// Every call validates on the host before it launches anything, in this order:
+//   1. the argument arrays themselves (NULL array -> INVALID_ARGUMENT)
+//   2. the session handle (dead or unknown -> MISSING_REGISTRATION)
+//   3. per-rank counts (SHAPE_MISMATCH), ops (INCONSISTENT_OP),
+//      roots (INCONSISTENT_ROOT), broadcast senders (BROADCAST_SENDERS)
+//   4. a count of 0 returns RCC_OK here (valid no-op)
+//   5. per-rank buffers (NULL -> MISSING_REGISTRATION: that rank did not
+//      take part)
+//   6. overlaps and other malformed arguments (INVALID_ARGUMENT)
+//   7. the current CUDA device against the session's (INVALID_ARGUMENT)
+// [ruCCL README §3 "Registration and call contract", §4 "Errors and
+// lifecycle"; Monarch "Struct Communicator": each call returns a status.]
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "rcc.h"
+#include "rcc_internal.h"
+
+namespace {
+
+using rcc::MultiPtrArgs;
+
+// ---- errors and counters ---------------------------------------------------
+
+thread_local std::string t_err;
+std::atomic<uint64_t> g_launches{0};
+
+rcc_status fail(rcc_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return st;
+}
+
+rcc_status cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();  // clear a sticky launch error so later calls can run
+  return fail(RCC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int wait_limit_ms() {
+  const char* v = std::getenv("RCC_WAIT_LIMIT_MS");
+  if (v && *v) {
+    int ms = std::atoi(v);
+    if (ms > 0) return ms;
+  }
+  return 120000;
+}
+
+// Wait for an event with a time limit: poll, yield, then back off with short
+// sleeps.  Never blocks forever.
+rcc_status wait_event(cudaEvent_t ev, const char* what) {
+  const auto t0 = std::chrono::steady_clock::now();
+  const int limit = wait_limit_ms();
+  for (long spins = 0;; ++spins) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return RCC_OK;
+    if (e != cudaErrorNotReady) return cuda_fail(e, what);
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                        std::chrono::steady_clock::now() - t0)
+                        .count();
+    if (ms > limit)
+      return fail(RCC_ERR_TIMEOUT, "%s: GPU work did not complete within %d ms", what, limit);
+    if (spins < 2000)
+      std::this_thread::yield();
+    else
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+// ---- sessions ----------------------------------------------------------------
+
+constexpr size_t kCombineRegionBytes = 49200;   // 4096 level-1 rows + 4 level-2 rows, 12 B each
+constexpr uint64_t kMaxStatsRows = 4096ull * 1024ull;
+constexpr uint32_t kDefaultElemsPerRow = 8192;
+constexpr uint64_t kFanIn = 1024;
+
+struct Scratch {
+  void* rows = nullptr;
+  size_t rows_cap = 0;
+  void* combine = nullptr;          // the reused reduction region, kCombineRegionBytes
+  uint32_t* report_dev = nullptr;   // 12-byte report (16 allocated)
+  uint32_t* report_host = nullptr;  // pinned readback slot
+  void* desc_dev = nullptr;         // tensor table + grad table + state table
+  size_t desc_cap = 0;
+  void* desc_host = nullptr;        // pinned staging for the tables
+  size_t desc_host_cap = 0;
+  std::vector<unsigned char> last_desc;  // bytes most recently uploaded
+  cudaEvent_t report_ev = nullptr;
+  cudaEvent_t done_ev = nullptr;    // end of the previous call's work
+  bool done_recorded = false;
+};
+
+struct Session {
+  int device;
+  int R;
+  rcc_dtype dtype;
+  std::atomic<unsigned> flags;
+  std::mutex mu;  // serialises scratch use and teardown
+  Scratch sc;
+  Session(int d, int r, rcc_dtype t, unsigned f) : device(d), R(r), dtype(t), flags(f) {}
+};
+
+void free_scratch(Scratch& s) {
+  if (s.rows) cudaFree(s.rows);
+  if (s.combine) cudaFree(s.combine);
+  if (s.report_dev) cudaFree(s.report_dev);
+  if (s.report_host) cudaFreeHost(s.report_host);
+  if (s.desc_dev) cudaFree(s.desc_dev);
+  if (s.desc_host) cudaFreeHost(s.desc_host);
+  if (s.report_ev) cudaEventDestroy(s.report_ev);
+  if (s.done_ev) cudaEventDestroy(s.done_ev);
+  s = Scratch{};
+}
+
+constexpr int kSlots = 255;
+struct Slot {
+  std::shared_ptr<Session> s;
+  uint32_t gen = 0;
+};
+std::mutex g_reg_mu;
+Slot g_slots[kSlots];
+
+rcc_comm encode(int slot, uint32_t gen) {
+  return reinterpret_cast<rcc_comm>(
+      static_cast<uintptr_t>((static_cast<uint64_t>(gen) << 8) | static_cast<uint64_t>(slot + 1)));
+}
+
+std::shared_ptr<Session> lookup(rcc_comm h, int* slot_out = nullptr) {
+  const uint64_t v = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(h));
+  if (v == 0) return nullptr;
+  const int slot = static_cast<int>(v & 0xFF) - 1;
+  const uint32_t gen = static_cast<uint32_t>(v >> 8);
+  if (slot < 0 || slot >= kSlots) return nullptr;
+  std::lock_guard<std::mutex> lock(g_reg_mu);
+  if (!g_slots[slot].s || g_slots[slot].gen != gen) return nullptr;
+  if (slot_out) *slot_out = slot;
+  return g_slots[slot].s;
+}
+
+// Remove a session from the registry; returns it (nullptr if already gone).
+std::shared_ptr<Session> unregister(rcc_comm h) {
+  int slot = -1;
+  auto s = lookup(h, &slot);
+  if (!s) return nullptr;
+  std::lock_guard<std::mutex> lock(g_reg_mu);
+  if (g_slots[slot].s != s) return nullptr;
+  g_slots[slot].s.reset();
+  return s;
+}
+
+rcc_status missing_session() {
+  return fail(RCC_ERR_MISSING_REGISTRATION,
+              "session handle is not registered (never registered, finished or reset)");
+}
+
+// ---- validation helpers ----------------------------------------------------
+
+size_t elem_bytes(rcc_dtype t) { return t == RCC_F32 ? 4 : 2; }
+bool valid_op(int op) { return op >= RCC_SUM && op <= RCC_MIN; }
+
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+  if (an == 0 || bn == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bn && y < x + an;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rcc_status check_counts(const size_t* counts, int R, size_t* n) {
+  for (int r = 1; r < R; ++r)
+    if (counts[r] != counts[0])
+      return fail(RCC_ERR_SHAPE_MISMATCH, "rank %d has %zu elements, rank 0 has %zu", r,
+                  counts[r], counts[0]);
+  *n = counts[0];
+  return RCC_OK;
+}
+
+rcc_status check_ops(const rcc_op* ops, int R) {
+  for (int r = 0; r < R; ++r) {
+    if (!valid_op(ops[r]))
+      return fail(RCC_ERR_INCONSISTENT_OP, "rank %d passes op %d, not an rcc_op", r, (int)ops[r]);
+    if (ops[r] != ops[0])
+      return fail(RCC_ERR_INCONSISTENT_OP, "rank %d passes op %d, rank 0 passes %d", r,
+                  (int)ops[r], (int)ops[0]);
+  }
+  return RCC_OK;
+}
+
+rcc_status check_device(int dev) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != dev)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "current CUDA device %d is not the session's device %d",
+                cur, dev);
+  return RCC_OK;
+}
+
+rcc::Red red_of(rcc_op op) {
+  switch (op) {
+    case RCC_MAX: return rcc::kRedMax;
+    case RCC_MIN: return rcc::kRedMin;
+    default: return rcc::kRedSum;
+  }
+}
+
+rcc_status launch(const Session& s, rcc::Red red, int nseg, const MultiPtrArgs& a,
+                  rcc_stream_t stream) {
+  const bool fast = (s.flags.load() & RCC_DETERMINISTIC) == 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = s.dtype == RCC_F32 ? rcc::launch_multi_ptr_f32(red, fast, nseg, a, st)
+                                     : rcc::launch_multi_ptr_bf16(red, fast, nseg, a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "collective kernel launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return RCC_OK;
+}
+
+// 16-byte vectors are usable when every base address is 16-byte aligned and
+// every per-segment offset keeps it so.
+int vec_ok(const MultiPtrArgs& a, int nsrc_ptrs, int ndst_ptrs, size_t seg_bytes_src,
+           size_t seg_bytes_dst) {
+  for (int i = 0; i < nsrc_ptrs; ++i)
+    if (!aligned16(a.src[i])) return 0;
+  for (int i = 0; i < ndst_ptrs; ++i)
+    if (!aligned16(a.dst[i])) return 0;
+  if (seg_bytes_src % 16 || seg_bytes_dst % 16) return 0;
+  return 1;
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+const char* rcc_last_error_message(void) { return t_err.c_str(); }
+
+const char* rcc_status_string(rcc_status st) {
+  switch (st) {
+    case RCC_OK: return "RCC_OK";
+    case RCC_ERR_DUPLICATE_REGISTRATION: return "RCC_ERR_DUPLICATE_REGISTRATION";
+    case RCC_ERR_MISSING_REGISTRATION: return "RCC_ERR_MISSING_REGISTRATION";
+    case RCC_ERR_SHAPE_MISMATCH: return "RCC_ERR_SHAPE_MISMATCH";
+    case RCC_ERR_INCONSISTENT_OP: return "RCC_ERR_INCONSISTENT_OP";
+    case RCC_ERR_INCONSISTENT_ROOT: return "RCC_ERR_INCONSISTENT_ROOT";
+    case RCC_ERR_BROADCAST_SENDERS: return "RCC_ERR_BROADCAST_SENDERS";
+    case RCC_ERR_INVALID_ARGUMENT: return "RCC_ERR_INVALID_ARGUMENT";
+    case RCC_ERR_TIMEOUT: return "RCC_ERR_TIMEOUT";
+    case RCC_ERR_CUDA: return "RCC_ERR_CUDA";
+  }
+  return "unknown rcc_status";
+}
+
+uint64_t rcc_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// ---- lifecycle ---------------------------------------------------------------
+
+rcc_status rcc_register(int device, int num_ranks, rcc_dtype dtype, unsigned flags,
+                        rcc_comm* out) {
+  t_err.clear();
+  if (!out) return fail(RCC_ERR_INVALID_ARGUMENT, "out is NULL");
+  *out = nullptr;
+  if (device < 0) return fail(RCC_ERR_INVALID_ARGUMENT, "device %d < 0", device);
+  if (num_ranks < 1 || num_ranks > RCC_MAX_RANKS)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "num_ranks %d outside [1, %d]", num_ranks,
+                RCC_MAX_RANKS);
+  if (dtype != RCC_F32 && dtype != RCC_BF16)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "dtype %d is not an rcc_dtype", (int)dtype);
+  if (flags & ~RCC_DETERMINISTIC)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags & ~RCC_DETERMINISTIC);
+  std::lock_guard<std::mutex> lock(g_reg_mu);
+  int free_slot = -1;
+  for (int i = 0; i < kSlots; ++i) {
+    if (g_slots[i].s) {
+      if (g_slots[i].s->device == device)
+        return fail(RCC_ERR_DUPLICATE_REGISTRATION,
+                    "device %d already has a live session (finish or reset it first)", device);
+    } else if (free_slot < 0) {
+      free_slot = i;
+    }
+  }
+  if (free_slot < 0) return fail(RCC_ERR_INVALID_ARGUMENT, "too many live sessions");
+  Slot& sl = g_slots[free_slot];
+  sl.gen = (sl.gen + 1) & 0x00FFFFFFu;
+  if (sl.gen == 0) sl.gen = 1;
+  sl.s = std::make_shared<Session>(device, num_ranks, dtype, flags);
+  *out = encode(free_slot, sl.gen);
+  return RCC_OK;
+}
+
+rcc_status rcc_set_flags(rcc_comm comm, unsigned flags) {
+  t_err.clear();
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  if (flags & ~RCC_DETERMINISTIC)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags & ~RCC_DETERMINISTIC);
+  s->flags.store(flags);
+  return RCC_OK;
+}
+
+rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream) {
+  t_err.clear();
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  {
+    std::lock_guard<std::mutex> lock(s->mu);
+    rcc_status st = check_device(s->device);
+    if (st != RCC_OK) return st;
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+    e = cudaEventRecord(ev, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+      cudaEventDestroy(ev);
+      return cuda_fail(e, "cudaEventRecord");
+    }
+    st = wait_event(ev, "rcc_finish");
+    cudaEventDestroy(ev);
+    if (st != RCC_OK) return st;  // the session stays live: retry or reset
+    free_scratch(s->sc);
+  }
+  unregister(comm);
+  return RCC_OK;
+}
+
+rcc_status rcc_reset(rcc_comm comm) {
+  t_err.clear();
+  auto s = unregister(comm);
+  if (!s) return missing_session();
+  std::lock_guard<std::mutex> lock(s->mu);
+  free_scratch(s->sc);
+  return RCC_OK;
+}
+
+// ---- collectives ---------------------------------------------------------------
+
+rcc_status rcc_all_reduce(rcc_comm comm, const void* const* send, void* const* recv,
+                          const size_t* counts, const rcc_op* ops, rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !counts || !ops)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv, counts and ops arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t n;
+  rcc_status st = check_counts(counts, R, &n);
+  if (st != RCC_OK) return st;
+  if ((st = check_ops(ops, R)) != RCC_OK) return st;
+  if (n == 0) return RCC_OK;
+  for (int r = 0; r < R; ++r)
+    if (!send[r] || !recv[r])
+      return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no %s buffer", r,
+                  send[r] ? "recv" : "send");
+  const size_t bytes = n * elem_bytes(s->dtype);
+  for (int r = 0; r < R; ++r)
+    for (int q = 0; q < R; ++q) {
+      if (q != r && overlap(recv[r], bytes, recv[q], bytes))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv buffers of ranks %d and %d overlap", r, q);
+      if (overlap(recv[r], bytes, send[q], bytes) && !(q == r && recv[r] == send[r]))
+        return fail(RCC_ERR_INVALID_ARGUMENT,
+                    "recv of rank %d overlaps send of rank %d (only recv[r] == send[r] may alias)",
+                    r, q);
+    }
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  MultiPtrArgs a{};
+  for (int r = 0; r < R; ++r) {
+    a.src[r] = send[r];
+    a.dst[r] = recv[r];
+  }
+  a.n = n;
+  a.nsrc = a.ndst = R;
+  a.mean_div = ops[0] == RCC_MEAN ? R : 0;
+  a.vec_ok = vec_ok(a, R, R, 0, 0);
+  return launch(*s, red_of(ops[0]), 1, a, stream);
+}
+
+rcc_status rcc_reduce(rcc_comm comm, const void* const* send, void* const* recv,
+                      const size_t* counts, const rcc_op* ops, const int* roots,
+                      rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !counts || !ops || !roots)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv, counts, ops and roots arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t n;
+  rcc_status st = check_counts(counts, R, &n);
+  if (st != RCC_OK) return st;
+  if ((st = check_ops(ops, R)) != RCC_OK) return st;
+  for (int r = 0; r < R; ++r) {
+    if (roots[r] < 0 || roots[r] >= R)
+      return fail(RCC_ERR_INCONSISTENT_ROOT, "rank %d names root %d outside [0, %d)", r, roots[r],
+                  R);
+    if (roots[r] != roots[0])
+      return fail(RCC_ERR_INCONSISTENT_ROOT, "rank %d names root %d, rank 0 names %d", r, roots[r],
+                  roots[0]);
+  }
+  if (n == 0) return RCC_OK;
+  const int root = roots[0];
+  for (int r = 0; r < R; ++r)
+    if (!send[r]) return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no send buffer", r);
+  if (!recv[root])
+    return fail(RCC_ERR_MISSING_REGISTRATION, "root rank %d supplies no recv buffer", root);
+  const size_t bytes = n * elem_bytes(s->dtype);
+  for (int q = 0; q < R; ++q)
+    if (overlap(recv[root], bytes, send[q], bytes) && !(q == root && recv[root] == send[root]))
+      return fail(RCC_ERR_INVALID_ARGUMENT, "root recv overlaps send of rank %d", q);
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  MultiPtrArgs a{};
+  for (int r = 0; r < R; ++r) a.src[r] = send[r];
+  a.dst[0] = recv[root];
+  a.n = n;
+  a.nsrc = R;
+  a.ndst = 1;
+  a.mean_div = ops[0] == RCC_MEAN ? R : 0;
+  a.vec_ok = vec_ok(a, R, 1, 0, 0);
+  return launch(*s, red_of(ops[0]), 1, a, stream);
+}
+
+rcc_status rcc_broadcast(rcc_comm comm, const void* const* send, void* const* recv,
+                         const size_t* counts, rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !counts)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and counts arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t n;
+  rcc_status st = check_counts(counts, R, &n);
+  if (st != RCC_OK) return st;
+  int senders = 0, root = -1;
+  for (int r = 0; r < R; ++r)
+    if (send[r]) {
+      ++senders;
+      root = r;
+    }
+  if (senders != 1)
+    return fail(RCC_ERR_BROADCAST_SENDERS, "broadcast needs exactly one sender, got %d", senders);
+  if (n == 0) return RCC_OK;
+  for (int r = 0; r < R; ++r)
+    if (r != root && !recv[r])
+      return fail(RCC_ERR_MISSING_REGISTRATION, "receiving rank %d supplies no recv buffer", r);
+  const size_t bytes = n * elem_bytes(s->dtype);
+  MultiPtrArgs a{};
+  int nd = 0;
+  for (int r = 0; r < R; ++r) {
+    if (!recv[r] || recv[r] == send[root]) continue;
+    if (overlap(recv[r], bytes, send[root], bytes))
+      return fail(RCC_ERR_INVALID_ARGUMENT, "recv of rank %d overlaps the root's send buffer", r);
+    for (int q = 0; q < r; ++q)
+      if (recv[q] && recv[q] != send[root] && overlap(recv[r], bytes, recv[q], bytes))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv buffers of ranks %d and %d overlap", q, r);
+    a.dst[nd++] = recv[r];
+  }
+  if (nd == 0) return RCC_OK;  // only the root, in place
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  a.src[0] = send[root];
+  a.n = n;
+  a.nsrc = 1;
+  a.ndst = nd;
+  a.vec_ok = vec_ok(a, 1, nd, 0, 0);
+  return launch(*s, rcc::kRedCopy, 1, a, stream);
+}
+
+rcc_status rcc_reduce_scatter(rcc_comm comm, const void* const* send, void* const* recv,
+                              const size_t* in_counts, const rcc_op* ops, rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !in_counts || !ops)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv, in_counts and ops arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t N;
+  rcc_status st = check_counts(in_counts, R, &N);
+  if (st != RCC_OK) return st;
+  if (N % (size_t)R != 0)
+    return fail(RCC_ERR_SHAPE_MISMATCH, "input count %zu is not a multiple of %d ranks", N, R);
+  if ((st = check_ops(ops, R)) != RCC_OK) return st;
+  if (N == 0) return RCC_OK;
+  for (int r = 0; r < R; ++r)
+    if (!send[r] || !recv[r])
+      return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no %s buffer", r,
+                  send[r] ? "recv" : "send");
+  const size_t es = elem_bytes(s->dtype), n = N / (size_t)R;
+  for (int r = 0; r < R; ++r)
+    for (int q = 0; q < R; ++q) {
+      if (q != r && overlap(recv[r], n * es, recv[q], n * es))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv buffers of ranks %d and %d overlap", r, q);
+      if (overlap(recv[r], n * es, send[q], N * es))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv of rank %d overlaps send of rank %d", r, q);
+    }
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  MultiPtrArgs a{};
+  for (int r = 0; r < R; ++r) {
+    a.src[r] = send[r];
+    a.dst[r] = recv[r];
+  }
+  a.n = n;
+  a.nsrc = R;
+  a.ndst = 1;
+  a.src_seg_stride = n;
+  a.dst_per_seg = 1;
+  a.mean_div = ops[0] == RCC_MEAN ? R : 0;
+  a.vec_ok = vec_ok(a, R, R, n * es, 0);
+  return launch(*s, red_of(ops[0]), R, a, stream);
+}
+
+rcc_status rcc_all_gather(rcc_comm comm, const void* const* send, void* const* recv,
+                          const size_t* in_counts, rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !in_counts)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and in_counts arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t n;
+  rcc_status st = check_counts(in_counts, R, &n);
+  if (st != RCC_OK) return st;
+  if (n == 0) return RCC_OK;
+  for (int r = 0; r < R; ++r)
+    if (!send[r] || !recv[r])
+      return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no %s buffer", r,
+                  send[r] ? "recv" : "send");
+  const size_t es = elem_bytes(s->dtype), N = n * (size_t)R;
+  for (int r = 0; r < R; ++r)
+    for (int q = 0; q < R; ++q) {
+      if (q != r && overlap(recv[r], N * es, recv[q], N * es))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv buffers of ranks %d and %d overlap", r, q);
+      // in place: rank q's input may be its own slot q of its own output
+      const bool own_slot =
+          q == r && send[q] == static_cast<const char*>(recv[r]) + (size_t)q * n * es;
+      if (overlap(recv[r], N * es, send[q], n * es) && !own_slot)
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv of rank %d overlaps send of rank %d", r, q);
+    }
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  MultiPtrArgs a{};
+  for (int r = 0; r < R; ++r) {
+    a.src[r] = send[r];
+    a.dst[r] = recv[r];
+  }
+  a.n = n;
+  a.nsrc = 1;
+  a.ndst = R;
+  a.src_per_seg = 1;
+  a.dst_seg_stride = n;
+  a.vec_ok = vec_ok(a, R, R, 0, n * es);
+  return launch(*s, rcc::kRedCopy, R, a, stream);
+}
+
+// ---- gradient sync + fused AdamW ------------------------------------------------
+
+}  // extern "C"
+
+namespace {
+
+template <typename T>
+rcc_status ensure_dev(T** p, size_t* cap, size_t need, const char* what) {
+  if (*p && *cap >= need) return RCC_OK;
+  if (*p) cudaFree(*p);
+  *p = nullptr;
+  *cap = 0;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), need);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  *cap = need;
+  return RCC_OK;
+}
+
+rcc_status ensure_fixed_scratch(Scratch& sc) {
+  cudaError_t e;
+  if (!sc.combine) {
+    e = cudaMalloc(&sc.combine, kCombineRegionBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(combine region)");
+  }
+  if (!sc.report_dev) {
+    e = cudaMalloc(reinterpret_cast<void**>(&sc.report_dev), 16);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(report)");
+  }
+  if (!sc.report_host) {
+    e = cudaMallocHost(reinterpret_cast<void**>(&sc.report_host), 16);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(report)");
+  }
+  if (!sc.report_ev) {
+    e = cudaEventCreateWithFlags(&sc.report_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  }
+  if (!sc.done_ev) {
+    e = cudaEventCreateWithFlags(&sc.done_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  }
+  return RCC_OK;
+}
+
+bool finite_pos(double x) { return std::isfinite(x) && x > 0.0; }
+
+}  // namespace
+
+extern "C" {
+
+rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int num_params,
+                               const rcc_adamw_cfg* cfg, rcc_optim_state* state,
+                               rcc_step_report* report, rcc_stream_t stream) {
+  t_err.clear();
+  if (!params || !cfg || !state || num_params < 1)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "params, cfg, state and num_params >= 1 are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  // shapes must match across ranks [ruCCL §6]
+  for (int p = 0; p < num_params; ++p) {
+    const rcc_param_set& ps = params[p];
+    if (ps.rank_numel)
+      for (int r = 0; r < R; ++r)
+        if (ps.rank_numel[r] != ps.numel)
+          return fail(RCC_ERR_SHAPE_MISMATCH, "tensor %d: rank %d has %zu elements, expected %zu",
+                      p, r, ps.rank_numel[r], ps.numel);
+  }
+  const int rep = cfg->replicas;
+  for (int p = 0; p < num_params; ++p) {
+    const rcc_param_set& ps = params[p];
+    if (!ps.grads)
+      return fail(RCC_ERR_MISSING_REGISTRATION, "tensor %d has no grads array", p);
+    for (int r = 0; r < R; ++r)
+      if (!ps.grads[r])
+        return fail(RCC_ERR_MISSING_REGISTRATION, "tensor %d: rank %d supplies no gradient", p, r);
+  }
+  if (s->dtype != RCC_F32)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "gradient sync needs an RCC_F32 session");
+  if (rep != 1 && rep != R)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "replicas %d must be 1 or %d", rep, R);
+  if (cfg->reserved != 0) return fail(RCC_ERR_INVALID_ARGUMENT, "cfg->reserved must be 0");
+  if (!finite_pos(cfg->lr) && cfg->lr != 0.0)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "lr must be finite and >= 0");
+  if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "betas must lie in [0, 1)");
+  if (!finite_pos(cfg->eps)) return fail(RCC_ERR_INVALID_ARGUMENT, "eps must be finite and > 0");
+  if (!std::isfinite(cfg->weight_decay) || !std::isfinite(cfg->max_grad_norm))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "weight_decay and max_grad_norm must be finite");
+  const uint32_t epr = cfg->elems_per_row ? cfg->elems_per_row : kDefaultElemsPerRow;
+  if (epr % 4 != 0 || epr > (1u << 24))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "elems_per_row %u must be a multiple of 4 in [4, 2^24]",
+                epr);
+  if (!finite_pos(state->scale))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "loss scale must be finite and > 0");
+  if (state->growth_interval < 1 || !finite_pos(state->growth_factor) ||
+      !finite_pos(state->backoff_factor) || state->step < 0)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "malformed optimizer/scaler state");
+  uint64_t total_rows = 0;
+  for (int p = 0; p < num_params; ++p) {
+    const rcc_param_set& ps = params[p];
+    if (ps.numel == 0) return fail(RCC_ERR_INVALID_ARGUMENT, "tensor %d has 0 elements", p);
+    if (!ps.params || !ps.exp_avg || !ps.exp_avg_sq)
+      return fail(RCC_ERR_INVALID_ARGUMENT, "tensor %d lacks params/exp_avg/exp_avg_sq arrays", p);
+    for (int k = 0; k < rep; ++k)
+      if (!ps.params[k] || !ps.exp_avg[k] || !ps.exp_avg_sq[k])
+        return fail(RCC_ERR_INVALID_ARGUMENT, "tensor %d: replica %d state pointer is NULL", p, k);
+    total_rows += (ps.numel + epr - 1) / epr;
+  }
+  if (total_rows > kMaxStatsRows)
+    return fail(RCC_ERR_INVALID_ARGUMENT,
+                "%llu statistics rows exceed %llu (two fan-in-1024 levels); raise elems_per_row",
+                (unsigned long long)total_rows, (unsigned long long)kMaxStatsRows);
+  rcc_status st = check_device(s->device);
+  if (st != RCC_OK) return st;
+
+  std::lock_guard<std::mutex> lock(s->mu);
+  Scratch& sc = s->sc;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = ensure_fixed_scratch(sc)) != RCC_OK) return st;
+  if ((st = ensure_dev(&sc.rows, &sc.rows_cap, (size_t)total_rows * 12, "cudaMalloc(rows)")) !=
+      RCC_OK)
+    return st;
+
+  // descriptor tables: tensors | grad pointers | state pointers
+  const size_t P = (size_t)num_params;
+  const size_t off_grads = P * sizeof(rcc::GsTensor);
+  const size_t off_state = off_grads + P * R * sizeof(void*);
+  const size_t desc_bytes = off_state + P * 3 * rep * sizeof(void*);
+  const bool dev_grew = !sc.desc_dev || sc.desc_cap < desc_bytes;
+  if ((st = ensure_dev(&sc.desc_dev, &sc.desc_cap, desc_bytes, "cudaMalloc(descriptors)")) !=
+      RCC_OK)
+    return st;
+  if (!sc.desc_host || sc.desc_host_cap < desc_bytes) {
+    if (sc.desc_host) cudaFreeHost(sc.desc_host);
+    sc.desc_host = nullptr;
+    cudaError_t e = cudaMallocHost(&sc.desc_host, desc_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(descriptors)");
+    sc.desc_host_cap = desc_bytes;
+  }
+  std::vector<unsigned char> desc(desc_bytes);
+  auto* tens = reinterpret_cast<rcc::GsTensor*>(desc.data());
+  auto* gtab = reinterpret_cast<const float**>(desc.data() + off_grads);
+  auto* stab = reinterpret_cast<float**>(desc.data() + off_state);
+  std::vector<int> upd_vec(P);
+  uint64_t row = 0;
+  for (size_t p = 0; p < P; ++p) {
+    const rcc_param_set& ps = params[p];
+    bool gv = ps.mean_grad == nullptr || aligned16(ps.mean_grad);
+    for (int r = 0; r < R; ++r) {
+      gtab[p * R + r] = ps.grads[r];
+      gv = gv && aligned16(ps.grads[r]);
+    }
+    rcc::GsTensor t{};
+    t.numel = ps.numel;
+    t.row_begin = row;
+    t.mean_grad = ps.mean_grad;
+    t.grad_slot = (uint32_t)(p * R);
+    t.vec_ok = gv ? 1u : 0u;
+    tens[p] = t;
+    row += (ps.numel + epr - 1) / epr;
+    bool uv = gv;
+    for (int k = 0; k < rep; ++k) {
+      stab[p * 3 * rep + k] = ps.params[k];
+      stab[p * 3 * rep + rep + k] = ps.exp_avg[k];
+      stab[p * 3 * rep + 2 * rep + k] = ps.exp_avg_sq[k];
+      uv = uv && aligned16(ps.params[k]) && aligned16(ps.exp_avg[k]) && aligned16(ps.exp_avg_sq[k]);
+    }
+    upd_vec[p] = uv ? 1 : 0;
+  }
+  // the previous call's update kernels may still read the tables
+  cudaError_t e;
+  if (sc.done_recorded) {
+    e = cudaStreamWaitEvent(cs, sc.done_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  if (dev_grew || sc.last_desc != desc) {
+    std::memcpy(sc.desc_host, desc.data(), desc_bytes);
+    e = cudaMemcpyAsync(sc.desc_dev, sc.desc_host, desc_bytes, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
+    sc.last_desc.swap(desc);
+  }
+  const char* dbase = static_cast<const char*>(sc.desc_dev);
+  const float inv_scale = (float)(1.0 / state->scale);
+
+  // statistics pass + hierarchy
+  rcc::GsStatsArgs ga{};
+  ga.tensors = reinterpret_cast<const rcc::GsTensor*>(dbase);
+  ga.grads = reinterpret_cast<const float* const*>(dbase + off_grads);
+  ga.rows = static_cast<uint32_t*>(sc.rows);
+  ga.total_rows = total_rows;
+  ga.num_tensors = (uint32_t)P;
+  ga.elems_per_row = epr;
+  ga.R = R;
+  ga.inv_scale = inv_scale;
+  if ((e = rcc::launch_gs_stats(ga, cs)) != cudaSuccess) return cuda_fail(e, "statistics kernel");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+
+  const uint32_t* src = static_cast<const uint32_t*>(sc.rows);
+  uint64_t rows = total_rows;
+  int levels = 0;
+  uint64_t region_bytes = 0;
+  if (cfg->hierarchical_stats) {
+    uint32_t* region = static_cast<uint32_t*>(sc.combine);
+    while (rows > kFanIn) {
+      // level 1 writes rows [0, 4096) of the region, level 2 rows [4096, 4100)
+      uint32_t* out = region + (levels == 0 ? 0 : 4096 * 3);
+      const uint64_t out_rows = (rows + kFanIn - 1) / kFanIn;
+      if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
+        return cuda_fail(e, "combine kernel");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      region_bytes = (levels == 0 ? 0 : 4096 * 12) + out_rows * 12;
+      src = out;
+      rows = out_rows;
+      ++levels;
+    }
+  }
+  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, cs)) != cudaSuccess)
+    return cuda_fail(e, "report kernel");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if ((e = cudaMemcpyAsync(sc.report_host, sc.report_dev, 12, cudaMemcpyDeviceToHost, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "report readback");
+  if ((e = cudaEventRecord(sc.report_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((st = wait_event(sc.report_ev, "12-byte report readback")) != RCC_OK) return st;
+
+  // host decision [RUDA docs, native PyTorch section]: skip on non-finite,
+  // clip after unscale when the global norm exceeds max_grad_norm
+  uint64_t bits = ((uint64_t)sc.report_host[1] << 32) | sc.report_host[0];
+  double sum_sq;
+  std::memcpy(&sum_sq, &bits, 8);
+  const uint32_t nonfinite = sc.report_host[2];
+  const double norm = std::sqrt(sum_sq);
+  const bool skip = nonfinite > 0 || !std::isfinite(norm);
+  float coef = 1.0f;
+  if (!skip && cfg->max_grad_norm > 0.0 && norm > cfg->max_grad_norm)
+    coef = (float)(cfg->max_grad_norm / norm);
+
+  rcc_step_report rep_out{};
+  rep_out.sum_sq = sum_sq;
+  rep_out.grad_norm = norm;
+  rep_out.scale_used = state->scale;
+  rep_out.nonfinite = nonfinite;
+  rep_out.skipped = skip ? 1 : 0;
+  rep_out.clip_coef = skip ? 1.0f : coef;
+  rep_out.combine_launches = levels;
+  rep_out.stats_rows = total_rows;
+  rep_out.combine_region_bytes = region_bytes;
+
+  if (skip) {
+    state->scale *= state->backoff_factor;
+    state->growth_tracker = 0;
+  } else {
+    const int64_t t = state->step + 1;
+    const double bc1 = 1.0 - std::pow(cfg->beta1, (double)t);
+    const double bc2 = 1.0 - std::pow(cfg->beta2, (double)t);
+    rcc::GsUpdateArgs ua{};
+    ua.s.step_size = (float)(cfg->lr / bc1);
+    ua.s.inv_bc2_sqrt = (float)(1.0 / std::sqrt(bc2));
+    ua.s.decay = (float)(1.0 - cfg->lr * cfg->weight_decay);
+    ua.s.beta1 = (float)cfg->beta1;
+    ua.s.one_minus_beta1 = (float)(1.0 - cfg->beta1);
+    ua.s.beta2 = (float)cfg->beta2;
+    ua.s.one_minus_beta2 = (float)(1.0 - cfg->beta2);
+    ua.s.eps = (float)cfg->eps;
+    ua.R = R;
+    ua.replicas = rep;
+    ua.inv_scale = inv_scale;
+    ua.clip_coef = coef;
+    // one update kernel per parameter tensor
+    for (size_t p = 0; p < P; ++p) {
+      ua.state = reinterpret_cast<float* const*>(dbase + off_state) + p * 3 * rep;
+      ua.mean_grad = params[p].mean_grad;
+      ua.grads = reinterpret_cast<const float* const*>(dbase + off_grads) + p * R;
+      ua.numel = params[p].numel;
+      ua.vec_ok = upd_vec[p];
+      if ((e = rcc::launch_gs_update(ua, cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    rep_out.update_launches = P;
+    state->step = t;
+    state->growth_tracker += 1;
+    if (state->growth_tracker >= state->growth_interval) {
+      state->scale *= state->growth_factor;
+      state->growth_tracker = 0;
+    }
+  }
+  if ((e = cudaEventRecord(sc.done_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  sc.done_recorded = true;
+  if (report) *report = rep_out;
+  return RCC_OK;
+}
+
+}  // extern "C"

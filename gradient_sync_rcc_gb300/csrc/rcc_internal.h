@@ -1,0 +1,104 @@
+// rcc_internal.h -- launch interface between the host layer (rcc_host.cpp)
+// and the CUDA kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace rcc {
+
+constexpr int kMaxRanks = 64;
+constexpr int kThreads = 256;  // every collective / grad-sync kernel block
+
+// Element-wise operation of a multi-pointer pass.
+enum Red : int { kRedSum = 0, kRedMax = 1, kRedMin = 2, kRedCopy = 3 };
+
+// One multi-pointer pass: for every segment s (blockIdx.y) and element i < n,
+//   y = red(src_0[i], ..., src_{nsrc-1}[i])  (sources of segment s)
+//   dst_d[i] = y for each destination d of segment s.
+// Sources of segment s: src[s] alone when src_per_seg, else src[0..nsrc) each
+// advanced by s * src_seg_stride elements.  Destinations likewise with
+// dst_per_seg / dst_seg_stride.  This one shape covers all five collectives:
+//   all_reduce      1 segment, R sources, R destinations
+//   reduce          1 segment, R sources, 1 destination (the root's)
+//   broadcast       1 segment, 1 source (root), R (or R-1) destinations
+//   reduce_scatter  R segments, R sources at offset s*n, destination recv[s]
+//   all_gather      R segments, source send[s], R destinations at offset s*n
+struct MultiPtrArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  size_t n;
+  size_t src_seg_stride;
+  size_t dst_seg_stride;
+  int nsrc;
+  int ndst;
+  int src_per_seg;
+  int dst_per_seg;
+  int mean_div;  // > 0: the sum is divided by this (IEEE division) before storing
+  int vec_ok;    // 1: every source/destination address (with segment offsets)
+                 //    is 16-byte aligned, so whole 16-byte vectors may be used
+};
+
+// One launch of the pass; fast selects the pairwise-tree sum.
+cudaError_t launch_multi_ptr_f32(Red red, bool fast, int nseg, const MultiPtrArgs& a,
+                                 cudaStream_t stream);
+cudaError_t launch_multi_ptr_bf16(Red red, bool fast, int nseg, const MultiPtrArgs& a,
+                                  cudaStream_t stream);
+
+// ---- gradient sync -------------------------------------------------------
+
+// Device-side description of one parameter tensor for the statistics kernel.
+struct GsTensor {
+  uint64_t numel;
+  uint64_t row_begin;       // first statistics row of this tensor
+  float* mean_grad;         // optional output of the unscaled mean gradient
+  uint32_t grad_slot;       // index of this tensor's R grad pointers in the grad table
+  uint32_t vec_ok;          // all R grads (and mean_grad) 16-byte aligned
+};
+
+struct GsStatsArgs {
+  const GsTensor* tensors;      // [num_tensors]
+  const float* const* grads;    // [num_tensors * R] grad pointer table
+  uint32_t* rows;               // [total_rows * 3]: {sum_sq lo, sum_sq hi, nonfinite}
+  uint64_t total_rows;
+  uint32_t num_tensors;
+  uint32_t elems_per_row;
+  int R;
+  float inv_scale;
+};
+
+// Statistics pass: one 12-byte row per block.
+cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);
+// One fan-in-1024 combine level: ceil(nrows / 1024) output rows.
+cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
+                              cudaStream_t stream);
+// Final reduction of nrows rows into the 12-byte report (one block).
+cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
+                             cudaStream_t stream);
+
+struct AdamWScalars {
+  float step_size;     // lr / (1 - beta1^t)
+  float inv_bc2_sqrt;  // 1 / sqrt(1 - beta2^t)
+  float decay;         // 1 - lr * wd
+  float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+};
+
+struct GsUpdateArgs {
+  float* const* state;          // this tensor's state pointer table (device memory):
+                                //   params[0..replicas), exp_avg[0..replicas), exp_avg_sq[0..replicas)
+  const float* mean_grad;       // unscaled mean gradient, or NULL
+  const float* const* grads;    // this tensor's R grads (device table), used when mean_grad is NULL
+  uint64_t numel;
+  int R;
+  int replicas;
+  int vec_ok;                   // every pointer 16-byte aligned
+  float inv_scale;
+  float clip_coef;
+  AdamWScalars s;
+};
+
+cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream);
+
+}  // namespace rcc

@@ -1,0 +1,277 @@
+"""Python binding of librcc's C ABI (include/rcc.h): argument marshalling only.
+
+Every collective and the gradient-sync step run inside librcc.so's CUDA
+kernels; this module turns torch tensors into device pointers, element
+counts and the current CUDA stream, calls the C entry point of the same name
+and raises RccError on a non-zero status.  There is no fallback: if
+librcc.so is missing, loading raises.
+
+Low-level `raw_*` helpers pass arbitrary per-rank arrays straight through and
+return the status code, for exercising the validation paths.
+"""
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librcc.so")
+
+# status codes, dtypes, ops, flags (mirrors include/rcc.h)
+OK = 0
+ERR_DUPLICATE_REGISTRATION = 1
+ERR_MISSING_REGISTRATION = 2
+ERR_SHAPE_MISMATCH = 3
+ERR_INCONSISTENT_OP = 4
+ERR_INCONSISTENT_ROOT = 5
+ERR_BROADCAST_SENDERS = 6
+ERR_INVALID_ARGUMENT = 7
+ERR_TIMEOUT = 8
+ERR_CUDA = 9
+F32, BF16 = 0, 1
+SUM, MEAN, MAX, MIN = 0, 1, 2, 3
+OPS = {"sum": SUM, "mean": MEAN, "max": MAX, "min": MIN}
+DETERMINISTIC = 0x1
+MAX_RANKS = 64
+
+# every symbol include/rcc.h declares
+SYMBOLS = ["rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
+           "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
+           "rcc_grad_sync_adamw", "rcc_last_error_message", "rcc_status_string",
+           "rcc_kernel_launch_count"]
+
+
+class ParamSet(C.Structure):
+    _fields_ = [("numel", C.c_size_t), ("rank_numel", C.POINTER(C.c_size_t)),
+                ("grads", C.POINTER(C.c_void_p)), ("params", C.POINTER(C.c_void_p)),
+                ("exp_avg", C.POINTER(C.c_void_p)), ("exp_avg_sq", C.POINTER(C.c_void_p)),
+                ("mean_grad", C.c_void_p)]
+
+
+class AdamWCfg(C.Structure):
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("eps", C.c_double), ("weight_decay", C.c_double),
+                ("max_grad_norm", C.c_double), ("replicas", C.c_int32),
+                ("hierarchical_stats", C.c_int32), ("elems_per_row", C.c_uint32),
+                ("reserved", C.c_uint32)]
+
+
+class OptimState(C.Structure):
+    _fields_ = [("step", C.c_int64), ("scale", C.c_double), ("growth_factor", C.c_double),
+                ("backoff_factor", C.c_double), ("growth_interval", C.c_int32),
+                ("growth_tracker", C.c_int32)]
+
+
+class StepReport(C.Structure):
+    _fields_ = [("sum_sq", C.c_double), ("grad_norm", C.c_double), ("scale_used", C.c_double),
+                ("nonfinite", C.c_uint32), ("skipped", C.c_int32), ("clip_coef", C.c_float),
+                ("combine_launches", C.c_int32), ("stats_rows", C.c_uint64),
+                ("combine_region_bytes", C.c_uint64), ("update_launches", C.c_uint64)]
+
+
+_lib = None
+_PP = C.POINTER(C.c_void_p)
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "librcc.so is not built (%s); build it with gradient_sync_rcc_gb300.build.build()"
+                % LIB_PATH)
+        L = C.CDLL(LIB_PATH)
+        st = C.c_int
+        L.rcc_register.argtypes = [C.c_int, C.c_int, C.c_int, C.c_uint, _PP]
+        L.rcc_set_flags.argtypes = [C.c_void_p, C.c_uint]
+        L.rcc_finish.argtypes = [C.c_void_p, C.c_void_p]
+        L.rcc_reset.argtypes = [C.c_void_p]
+        L.rcc_all_reduce.argtypes = [C.c_void_p, _PP, _PP, C.POINTER(C.c_size_t),
+                                     C.POINTER(C.c_int), C.c_void_p]
+        L.rcc_reduce.argtypes = [C.c_void_p, _PP, _PP, C.POINTER(C.c_size_t),
+                                 C.POINTER(C.c_int), C.POINTER(C.c_int), C.c_void_p]
+        L.rcc_broadcast.argtypes = [C.c_void_p, _PP, _PP, C.POINTER(C.c_size_t), C.c_void_p]
+        L.rcc_reduce_scatter.argtypes = [C.c_void_p, _PP, _PP, C.POINTER(C.c_size_t),
+                                         C.POINTER(C.c_int), C.c_void_p]
+        L.rcc_all_gather.argtypes = [C.c_void_p, _PP, _PP, C.POINTER(C.c_size_t), C.c_void_p]
+        L.rcc_grad_sync_adamw.argtypes = [C.c_void_p, C.POINTER(ParamSet), C.c_int,
+                                          C.POINTER(AdamWCfg), C.POINTER(OptimState),
+                                          C.POINTER(StepReport), C.c_void_p]
+        for name in ("rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
+                     "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
+                     "rcc_grad_sync_adamw"):
+            getattr(L, name).restype = st
+        L.rcc_last_error_message.restype = C.c_char_p
+        L.rcc_last_error_message.argtypes = []
+        L.rcc_status_string.restype = C.c_char_p
+        L.rcc_status_string.argtypes = [C.c_int]
+        L.rcc_kernel_launch_count.restype = C.c_uint64
+        L.rcc_kernel_launch_count.argtypes = []
+        _lib = L
+    return _lib
+
+
+class RccError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        name = lib().rcc_status_string(status).decode()
+        super().__init__("%s: %s" % (name, message))
+
+
+def last_error():
+    return lib().rcc_last_error_message().decode()
+
+
+def _check(status):
+    if status != OK:
+        raise RccError(status, last_error())
+    return status
+
+
+def launch_count():
+    return int(lib().rcc_kernel_launch_count())
+
+
+# ------------------------------------------------------------- marshalling
+
+def ptr_array(ptrs):
+    return (C.c_void_p * len(ptrs))(*[None if p is None or p == 0 else int(p) for p in ptrs])
+
+
+def size_array(vals):
+    return (C.c_size_t * len(vals))(*vals)
+
+
+def int_array(vals):
+    return (C.c_int * len(vals))(*vals)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _op(op):
+    return OPS[op] if isinstance(op, str) else int(op)
+
+
+# ------------------------------------------------------------- sessions
+
+def register(device=0, num_ranks=4, dtype=F32, deterministic=True):
+    """rcc_register; returns the session handle (an int)."""
+    h = C.c_void_p()
+    flags = DETERMINISTIC if deterministic else 0
+    _check(lib().rcc_register(device, num_ranks, dtype, flags, C.byref(h)))
+    return h.value
+
+
+def set_flags(comm, deterministic=True):
+    _check(lib().rcc_set_flags(comm, DETERMINISTIC if deterministic else 0))
+
+
+def finish(comm, stream=None):
+    _check(lib().rcc_finish(comm, _stream(stream)))
+
+
+def reset(comm):
+    _check(lib().rcc_reset(comm))
+
+
+# ------------------------------------------------------------- collectives (torch tensors)
+
+def all_reduce(comm, send, recv, op="sum", stream=None):
+    R = len(send)
+    _check(lib().rcc_all_reduce(comm, ptr_array([_ptr(t) for t in send]),
+                                ptr_array([_ptr(t) for t in recv]),
+                                size_array([t.numel() for t in send]),
+                                int_array([_op(op)] * R), _stream(stream)))
+
+
+def reduce(comm, send, recv_root, root, op="sum", stream=None):
+    R = len(send)
+    recv = [None] * R
+    recv[root] = recv_root
+    _check(lib().rcc_reduce(comm, ptr_array([_ptr(t) for t in send]),
+                            ptr_array([_ptr(t) for t in recv]),
+                            size_array([t.numel() for t in send]), int_array([_op(op)] * R),
+                            int_array([root] * R), _stream(stream)))
+
+
+def broadcast(comm, root_send, recv, root, stream=None):
+    R = len(recv)
+    send = [None] * R
+    send[root] = root_send
+    _check(lib().rcc_broadcast(comm, ptr_array([_ptr(t) for t in send]),
+                               ptr_array([_ptr(t) for t in recv]),
+                               size_array([root_send.numel()] * R), _stream(stream)))
+
+
+def reduce_scatter(comm, send, recv, op="sum", stream=None):
+    R = len(send)
+    _check(lib().rcc_reduce_scatter(comm, ptr_array([_ptr(t) for t in send]),
+                                    ptr_array([_ptr(t) for t in recv]),
+                                    size_array([t.numel() for t in send]),
+                                    int_array([_op(op)] * R), _stream(stream)))
+
+
+def all_gather(comm, send, recv, stream=None):
+    _check(lib().rcc_all_gather(comm, ptr_array([_ptr(t) for t in send]),
+                                ptr_array([_ptr(t) for t in recv]),
+                                size_array([t.numel() for t in send]), _stream(stream)))
+
+
+# ------------------------------------------------------------- gradient sync
+
+def adamw_cfg(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=1.0,
+              replicas=1, hierarchical_stats=True, elems_per_row=0):
+    return AdamWCfg(lr, betas[0], betas[1], eps, weight_decay, max_grad_norm, replicas,
+                    1 if hierarchical_stats else 0, elems_per_row, 0)
+
+
+def optim_state(scale=65536.0, growth_factor=2.0, backoff_factor=0.5, growth_interval=2000,
+                step=0):
+    return OptimState(step, scale, growth_factor, backoff_factor, growth_interval, 0)
+
+
+class ParamSets:
+    """Keeps the ctypes arrays of a list of parameter tensors alive.
+
+    tensors: list of dicts with keys grads (R tensors), params, exp_avg,
+    exp_avg_sq (replica lists) and optional mean_grad."""
+
+    def __init__(self, tensors):
+        self._keep = []
+        self.arr = (ParamSet * len(tensors))()
+        for i, t in enumerate(tensors):
+            g = ptr_array([x.data_ptr() for x in t["grads"]])
+            p = ptr_array([x.data_ptr() for x in t["params"]])
+            m = ptr_array([x.data_ptr() for x in t["exp_avg"]])
+            v = ptr_array([x.data_ptr() for x in t["exp_avg_sq"]])
+            self._keep += [g, p, m, v]
+            mg = t.get("mean_grad")
+            self.arr[i] = ParamSet(t["params"][0].numel(), None, g, p, m, v,
+                                   None if mg is None else mg.data_ptr())
+
+    def __len__(self):
+        return len(self.arr)
+
+
+def grad_sync_adamw(comm, param_sets, cfg, state, stream=None):
+    """rcc_grad_sync_adamw over a ParamSets; updates `state` in place and
+    returns the StepReport."""
+    rep = StepReport()
+    _check(lib().rcc_grad_sync_adamw(comm, param_sets.arr, len(param_sets), C.byref(cfg),
+                                     C.byref(state), C.byref(rep), _stream(stream)))
+    return rep
+
+
+# ------------------------------------------------------------- raw calls (status only)
+
+def raw(name, *args):
+    return getattr(lib(), name)(*args)

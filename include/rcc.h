@@ -1,0 +1,249 @@
+/*
+ * rcc.h -- C ABI of librcc: tensor collectives over R logical ranks whose
+ * buffers all live on one GPU, and the gradient-sync + fused AdamW step that
+ * consumes them.
+ *
+ * Sources (page title, section):
+ *   [ruCCL]   ruCCL README (ja): §2 "Tensor collective API" (register,
+ *             all_reduce, broadcast, reduce, finish_collective,
+ *             reset_collective), §3 "Registration and call contract",
+ *             §4 "Errors and lifecycle", §5 "CUDA example" (4 logical ranks on
+ *             GPU 0), §6 "Collective training" (all_reduce Mean of gradients,
+ *             then optimizer.step).
+ *   [RUDA-T]  RUDA docs "Training and saving state", section "Native PyTorch
+ *             training on ruda:0": ruda_torch.AdamW(fused_step, max_grad_norm,
+ *             hierarchical_stats), the 12-byte report read back before the
+ *             update, skip on non-finite gradients, FP32 master weights and
+ *             moments, one update kernel per parameter, fan-in-1024 statistics
+ *             with at most two extra combine kernels and a reused reduction
+ *             region of at most 49,200 bytes; ruda_torch.GradScaler.
+ *   [Monarch] "Struct Communicator" (torch_sys_cuda::nccl): all_reduce,
+ *             broadcast, reduce, all_gather_into_tensor, reduce_scatter_tensor,
+ *             each issued on a stream, each returning a status.
+ *
+ * Conventions shared by every call:
+ *   - Buffers are device memory on the session's GPU, owned by the caller.
+ *     Per-rank arguments are arrays of R entries indexed by logical rank.
+ *   - Calls validate everything on the host first (in the order of the
+ *     status codes below) and launch nothing when they return an error.
+ *   - Collectives are asynchronous on `stream`: they enqueue kernels and
+ *     return without synchronising.  rcc_grad_sync_adamw synchronises once,
+ *     to read its 12-byte report back.
+ *   - Inputs are never written, except where a call documents an in-place
+ *     form.  Outputs must not overlap each other or any input otherwise.
+ *   - The current CUDA device must be the session's device.
+ *   - Error text for the calling thread: rcc_last_error_message().
+ */
+#ifndef RCC_H
+#define RCC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* rcc_stream_t;
+
+#define RCC_MAX_RANKS 64
+
+/* [ruCCL §4]: CollectiveError covers duplicate or missing registration, shape
+ * mismatch, inconsistent reduction op or root, and an invalid broadcast
+ * sender count; [Monarch] calls return a status or an error. */
+typedef enum {
+  RCC_OK = 0,
+  RCC_ERR_DUPLICATE_REGISTRATION = 1, /* a live session already exists on that device */
+  RCC_ERR_MISSING_REGISTRATION = 2,   /* dead handle, or a rank's required buffer is NULL */
+  RCC_ERR_SHAPE_MISMATCH = 3,         /* per-rank counts differ; reduce_scatter count % R != 0 */
+  RCC_ERR_INCONSISTENT_OP = 4,        /* per-rank ops differ, or an op is not an rcc_op */
+  RCC_ERR_INCONSISTENT_ROOT = 5,      /* per-rank roots differ, or root outside [0, R) */
+  RCC_ERR_BROADCAST_SENDERS = 6,      /* broadcast with a number of senders other than 1 */
+  RCC_ERR_INVALID_ARGUMENT = 7,       /* anything else malformed (NULL array, bad dtype, overlap, ...) */
+  RCC_ERR_TIMEOUT = 8,                /* a bounded wait for the GPU ran out */
+  RCC_ERR_CUDA = 9                    /* a CUDA runtime call failed */
+} rcc_status;
+
+typedef enum { RCC_F32 = 0, RCC_BF16 = 1 } rcc_dtype;
+
+/* Reduction operations.  [ruCCL §6] names Mean; sum, max and min complete the
+ * set.  Arithmetic is fp32 for both dtypes (bf16 is widened exactly and the
+ * result rounded once to nearest-even).  MEAN = fl32(sum / R).  MAX/MIN keep
+ * the lowest rank's value among equals and return the quiet NaN 0x7FC00000
+ * (bf16 0x7FC0) when any input is NaN. */
+typedef enum { RCC_SUM = 0, RCC_MEAN = 1, RCC_MAX = 2, RCC_MIN = 3 } rcc_op;
+
+/* Session flags.  RCC_DETERMINISTIC: sums fold ranks in the fixed order
+ * 0, 1, ..., R-1 (acc = x0; acc = fl32(acc + x_r)), bit-identical to that
+ * definition.  Without it sums use a pairwise tree over ranks (same traffic,
+ * shorter dependency chain, results within the fp32 error bound).  MAX and
+ * MIN are exact in both modes. */
+#define RCC_DETERMINISTIC 0x1u
+
+/* Opaque session handle.  A finished or reset handle stays detectable: calls
+ * on it return RCC_ERR_MISSING_REGISTRATION, never touch freed memory. */
+typedef struct rcc_comm_s* rcc_comm;
+
+/* ---- session lifecycle --------------------------------------------------- */
+
+/* [ruCCL §2 register, §3: participants agree on the device count; §5: four
+ * logical ranks on GPU 0].  Registers num_ranks (1..RCC_MAX_RANKS) logical
+ * ranks on CUDA device `device` with element type `dtype`.  One live session
+ * per device ("the local collective service", [ruCCL §2 reset_collective]);
+ * a second registration on that device returns
+ * RCC_ERR_DUPLICATE_REGISTRATION.  Makes no CUDA call: session scratch is
+ * allocated on first use.  *out receives the handle. */
+rcc_status rcc_register(int device, int num_ranks, rcc_dtype dtype,
+                        unsigned flags, rcc_comm* out);
+
+/* Replace the session flags (e.g. switch RCC_DETERMINISTIC) for later calls. */
+rcc_status rcc_set_flags(rcc_comm comm, unsigned flags);
+
+/* [ruCCL §2 finish_collective, §4 "normal termination"].  Waits for work
+ * enqueued on `stream` (bounded: RCC_ERR_TIMEOUT after the limit), frees the
+ * session's scratch and ends the session. */
+rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream);
+
+/* [ruCCL §2 reset_collective, §4: discards registration and in-flight
+ * operation state; completes nothing, checkpoints nothing, recovers nothing].
+ * Ends the session at once.  Kernels already enqueued run to completion on
+ * the GPU (freeing the scratch waits for them); their results are not
+ * reported.  A new rcc_register on the device succeeds afterwards. */
+rcc_status rcc_reset(rcc_comm comm);
+
+/* ---- collectives ---------------------------------------------------------
+ * Every call: send/recv are arrays of R device pointers; counts, ops, roots
+ * are arrays of R per-rank values that must agree ([ruCCL §3]: shape,
+ * reduction op, root and other parameters must match).  A count of 0 is a
+ * valid no-op.  Element type is the session's dtype. */
+
+/* [ruCCL §2 all_reduce; §5 sum/mean with inputs unchanged; Monarch
+ * all_reduce].  recv[r][i] = op(send[0][i], ..., send[R-1][i]) for every
+ * rank r, i < counts[r].  Out of place; recv[r] == send[r] (in place) is also
+ * accepted. */
+rcc_status rcc_all_reduce(rcc_comm comm, const void* const* send,
+                          void* const* recv, const size_t* counts,
+                          const rcc_op* ops, rcc_stream_t stream);
+
+/* [ruCCL §2 reduce: non-root participants receive nothing; Monarch reduce].
+ * recv[root][i] = op_q send[q][i].  Only recv[root] is used (other entries
+ * may be NULL and are never written).  recv[root] == send[root] (in place) is
+ * accepted. */
+rcc_status rcc_reduce(rcc_comm comm, const void* const* send,
+                      void* const* recv, const size_t* counts,
+                      const rcc_op* ops, const int* roots,
+                      rcc_stream_t stream);
+
+/* [ruCCL §2 broadcast: the sender passes Some(tensor), receivers None; §3:
+ * each broadcast has exactly one sender; Monarch broadcast].  Exactly one
+ * send[r] is non-NULL: that rank is the root.  recv[r][i] = send[root][i]
+ * for every rank r whose recv[r] is non-NULL and not send[root] itself;
+ * every non-root rank must supply recv[r]. */
+rcc_status rcc_broadcast(rcc_comm comm, const void* const* send,
+                         void* const* recv, const size_t* counts,
+                         rcc_stream_t stream);
+
+/* [Monarch reduce_scatter_tensor: reduce, then scatter].  in_counts[r] = N
+ * elements per rank input, N % R == 0, shard n = N / R.
+ * recv[r][j] = op_q send[q][r*n + j] for j < n (recv[r] holds n elements). */
+rcc_status rcc_reduce_scatter(rcc_comm comm, const void* const* send,
+                              void* const* recv, const size_t* in_counts,
+                              const rcc_op* ops, rcc_stream_t stream);
+
+/* [Monarch all_gather_into_tensor].  in_counts[r] = n elements per rank
+ * input; recv[r] holds R*n elements: recv[r][q*n + j] = send[q][j]. */
+rcc_status rcc_all_gather(rcc_comm comm, const void* const* send,
+                          void* const* recv, const size_t* in_counts,
+                          rcc_stream_t stream);
+
+/* ---- gradient sync + fused AdamW ----------------------------------------- */
+
+/* One parameter tensor as seen by every rank. */
+typedef struct {
+  size_t numel;                /* elements per rank (> 0) */
+  const size_t* rank_numel;    /* optional [R]: each rank's own element count; all must
+                                  equal numel ([ruCCL §6]: gradient shapes must match
+                                  across ranks), else RCC_ERR_SHAPE_MISMATCH; NULL: skip */
+  const float* const* grads;   /* [R] rank r's loss-scaled fp32 gradient; read only */
+  float* const* params;        /* [replicas] fp32 master parameters, updated in place */
+  float* const* exp_avg;       /* [replicas] fp32 first moments m, updated in place */
+  float* const* exp_avg_sq;    /* [replicas] fp32 second moments v, updated in place */
+  float* mean_grad;            /* optional [numel]: receives the unscaled mean gradient;
+                                  NULL: not stored (the update re-reads the R grads) */
+} rcc_param_set;
+
+/* ruda_torch.AdamW options [RUDA-T] plus the published AdamW constants. */
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay;
+  double max_grad_norm;        /* > 0: clip when the global L2 norm exceeds it; <= 0: off */
+  int32_t replicas;            /* optimizer-state copies: 1 or R (each rank its own) */
+  int32_t hierarchical_stats;  /* 1: fan-in-1024 combines; 0: one flat final reduction */
+  uint32_t elems_per_row;      /* elements summarised per statistics row; 0 = 8192;
+                                  otherwise a multiple of 4 in [4, 2^24] */
+  uint32_t reserved;           /* must be 0 */
+} rcc_adamw_cfg;
+
+/* Optimizer step count and GradScaler state, owned by the caller, updated by
+ * each call ([RUDA-T]: scale -> step -> update on the same GradScaler). */
+typedef struct {
+  int64_t step;                /* applied AdamW steps t (skipped steps do not count) */
+  double scale;                /* loss scale S the gradients carry */
+  double growth_factor;        /* S *= growth_factor after growth_interval finite steps */
+  double backoff_factor;       /* S *= backoff_factor on a skipped step */
+  int32_t growth_interval;
+  int32_t growth_tracker;      /* consecutive finite steps since the last change */
+} rcc_optim_state;
+
+/* What one call did. */
+typedef struct {
+  double sum_sq;               /* sum of g^2 over finite unscaled mean gradients (fp64) */
+  double grad_norm;            /* sqrt(sum_sq) */
+  double scale_used;           /* the loss scale the gradients were divided by */
+  uint32_t nonfinite;          /* non-finite unscaled mean gradient elements */
+  int32_t skipped;             /* 1: whole step skipped (state untouched) */
+  float clip_coef;             /* multiplier applied to g (1 when not clipped) */
+  int32_t combine_launches;    /* extra hierarchical combine kernels (0..2) */
+  uint64_t stats_rows;         /* rows written by the statistics kernel */
+  uint64_t combine_region_bytes; /* bytes of the reused reduction region touched (<= 49,200) */
+  uint64_t update_launches;    /* AdamW update kernels launched (num_params or 0) */
+} rcc_step_report;
+
+/* [ruCCL §6 + RUDA-T].  One data-parallel optimizer step over num_params
+ * tensors:
+ *   1. all_reduce Mean of the R loss-scaled gradients in rank order, then
+ *      unscale: g = fl32(fl32(sum_q grads[q]) / R) * fl32(1 / S);
+ *   2. read-only analysis: sum of g^2 (fp64) and a count of non-finite g,
+ *      one 12-byte row per statistics block, fan-in-1024 combines (none for
+ *      <= 1024 rows, at most two), a 12-byte report in device memory;
+ *   3. the report is read back (the call's one synchronisation);
+ *   4. any non-finite g (or norm) skips the whole step: parameters, moments
+ *      and step count are untouched, S backs off;
+ *   5. otherwise clip_coef = max_grad_norm / ||g|| when ||g|| > max_grad_norm,
+ *      t = step + 1, and one AdamW update kernel per tensor updates every
+ *      replica: p = p*(1 - lr*wd); m = b1*m + (1-b1)*g'; v = b2*v + (1-b2)*g'^2;
+ *      p -= lr/(1-b1^t) * m / (sqrt(v)/sqrt(1-b2^t) + eps), g' = g*clip_coef;
+ *      S grows after growth_interval finite steps.
+ * Session dtype must be RCC_F32.  Gradients are never written.  `state` is
+ * read and updated; `report` (may be NULL) receives what happened.  Returns
+ * RCC_ERR_TIMEOUT if the report did not arrive within the wait limit. */
+rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params,
+                               int num_params, const rcc_adamw_cfg* cfg,
+                               rcc_optim_state* state, rcc_step_report* report,
+                               rcc_stream_t stream);
+
+/* ---- diagnostics ---------------------------------------------------------- */
+
+/* Message describing the calling thread's most recent error ("" if none). */
+const char* rcc_last_error_message(void);
+
+/* Fixed name of a status code. */
+const char* rcc_status_string(rcc_status status);
+
+/* Number of kernels this library has launched in the process so far. */
+uint64_t rcc_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RCC_H */

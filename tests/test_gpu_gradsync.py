@@ -1,0 +1,275 @@
+"""GPU parity of the gradient-sync + fused AdamW step against the CPU oracle.
+
+[ruCCL README §6]: all_reduce Mean of the gradients, then the optimizer step.
+[RUDA docs "Training and saving state", native PyTorch section]: unscale,
+read-only analysis, global L2 clip at max_grad_norm, fan-in-1024 statistics
+(no extra combine for <= 1024 rows, at most two, a reused region of at most
+49,200 bytes), the 12-byte report read back, skip on non-finite, FP32 master
+weights and moments, one update kernel per parameter.
+
+Acceptance: parameters (and moments) within 1e-6 relative of the oracle,
+|p_gpu - p_orc| <= 1e-6 * max(|p_orc|, 1e-3), after every step of a 10-step
+run with one NaN injected at step 7 (that step skipped, the scale halved);
+the sum of squares within 1e-12 relative; decisions and counters exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gradient_sync_rcc_gb300 import rcc, synth
+from gpu_util import DEV, bits_equal, session, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+LR, B1, B2, EPS, WD, MAXN = 1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0
+REL = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gradient_sync_rcc_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def close(gpu, ref):
+    return bool(np.all(np.abs(gpu.astype(np.float64) - ref) <= REL * np.maximum(np.abs(ref), 1e-3)))
+
+
+class Problem:
+    """Device state (replicas of p, m, v), persistent grad buffers, and the
+    oracle's single host copy of the same state."""
+
+    def __init__(self, R, sizes, seed, replicas, mean_grad=True):
+        self.R, self.sizes, self.seed, self.rep = R, sizes, seed, replicas
+        p0 = [synth.normal(n, 0.02, seed, 1, i) for i, n in enumerate(sizes)]
+        self.hp = [x.copy() for x in p0]
+        self.hm = [np.zeros(n, np.float32) for n in sizes]
+        self.hv = [np.zeros(n, np.float32) for n in sizes]
+        self.tensors = []
+        for i, n in enumerate(sizes):
+            self.tensors.append(dict(
+                grads=[torch.empty(n, device=DEV) for _ in range(R)],
+                params=[to_dev(p0[i]) for _ in range(replicas)],
+                exp_avg=[torch.zeros(n, device=DEV) for _ in range(replicas)],
+                exp_avg_sq=[torch.zeros(n, device=DEV) for _ in range(replicas)],
+                mean_grad=torch.empty(n, device=DEV) if mean_grad else None))
+        self.sets = rcc.ParamSets(self.tensors)
+
+    def host_grads(self, step, scale, nan_at=None):
+        out = []
+        for i, n in enumerate(self.sizes):
+            per = [(synth.normal(n, 1e-3, self.seed, 2, i, step, r) * np.float32(scale))
+                   .astype(np.float32) for r in range(self.R)]
+            out.append(per)
+        if nan_at is not None and step == nan_at:
+            out[0][0][0] = np.nan
+        return out
+
+    def load_grads(self, grads):
+        for i, per in enumerate(grads):
+            for r in range(self.R):
+                self.tensors[i]["grads"][r].copy_(to_dev(per[r]))
+
+
+def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0):
+    cfg = rcc.adamw_cfg(lr=LR, betas=(B1, B2), eps=EPS, weight_decay=WD, max_grad_norm=MAXN,
+                        replicas=prob.rep, **cfg_kw)
+    state = rcc.optim_state(scale=scale)
+    sc = orc.scaler_new(scale)
+    ostep = 0
+    reports = []
+    with session(prob.R, rcc.F32, True) as h:
+        for k in range(1, steps + 1):
+            grads = prob.host_grads(k, state.scale, nan_at)
+            assert state.scale == sc.scale
+            prob.load_grads(grads)
+            rep = rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+            torch.cuda.synchronize()
+            ostep, st, d = orc.grad_sync_adamw_step(
+                grads, prob.hp, prob.hm, prob.hv, lr=LR, beta1=B1, beta2=B2, eps=EPS,
+                weight_decay=WD, max_grad_norm=MAXN, step=ostep, scaler=sc)
+            reports.append(rep)
+            assert rep.skipped == d.skip
+            assert rep.nonfinite == st.nonfinite
+            assert state.step == ostep and state.scale == sc.scale
+            if not d.skip:
+                want = orc.stats_value(st)
+                assert abs(rep.sum_sq - want) <= 1e-12 * want, (rep.sum_sq, want)
+                assert abs(rep.clip_coef - d.clip_coef) <= 2e-7 * d.clip_coef
+                assert rep.update_launches == len(prob.sizes)
+            else:
+                assert rep.update_launches == 0
+            if check_each or k == steps:
+                for i in range(len(prob.sizes)):
+                    t = prob.tensors[i]
+                    p0 = to_host(t["params"][0])
+                    assert close(p0, prob.hp[i]), (k, i)
+                    assert close(to_host(t["exp_avg"][0]), prob.hm[i]), (k, i)
+                    assert close(to_host(t["exp_avg_sq"][0]), prob.hv[i]), (k, i)
+                    for j in range(1, prob.rep):
+                        assert torch.equal(t["params"][j], t["params"][0])
+                        assert torch.equal(t["exp_avg_sq"][j], t["exp_avg_sq"][0])
+    return reports, state
+
+
+@pytest.mark.parametrize("replicas", [1, 4])
+@pytest.mark.parametrize("mean_grad", [True, False])
+def test_ten_steps_nan_at_seven(orc, replicas, mean_grad):
+    sizes = synth.param_sizes(16, 1024, 65536, 10)
+    prob = Problem(4, sizes, 11, replicas, mean_grad)
+    reports, state = run_steps(orc, prob, 10, 7, {})
+    assert [r.skipped for r in reports] == [0] * 6 + [1] + [0] * 3
+    assert state.step == 9 and state.scale == 32768.0
+    assert all(r.combine_launches == 0 for r in reports)      # <= 1024 rows
+    assert all(r.clip_coef < 1.0 for r in reports if not r.skipped)
+
+
+def test_mean_grad_output_bitwise(orc):
+    R = 4
+    sizes = [1, 3, 4099, 70001]
+    prob = Problem(R, sizes, 12, 1, True)
+    grads = prob.host_grads(1, 65536.0)
+    prob.load_grads(grads)
+    cfg = rcc.adamw_cfg(replicas=1)
+    with session(R) as h:
+        rcc.grad_sync_adamw(h, prob.sets, cfg, rcc.optim_state())
+        torch.cuda.synchronize()
+    inv = np.float32(1.0 / 65536.0)
+    for i in range(len(sizes)):
+        want = orc.mean_unscale(grads[i], inv)
+        assert bits_equal(to_host(prob.tensors[i]["mean_grad"]), want)
+
+
+def _levels(rows):
+    return 0 if rows <= 1024 else (1 if rows <= 1024 * 1024 else 2)
+
+
+@pytest.mark.parametrize("epr,sizes", [
+    (8192, [5000, 70000]),                 # few rows: no combine
+    (64, [300000, 123457]),                # > 1024 rows: one combine level
+    (4, [3000000, 1500001]),               # > 1024^2 rows: two combine levels
+])
+def test_hierarchy_levels_and_region_bound(orc, epr, sizes):
+    prob = Problem(2, sizes, 13, 1, True)
+    reports, _ = run_steps(orc, prob, 2, None, {"elems_per_row": epr}, check_each=True)
+    rows = sum(-(-n // epr) for n in sizes)
+    for r in reports:
+        assert r.stats_rows == rows
+        assert r.combine_launches == _levels(rows)
+        assert r.combine_launches <= 2
+        assert r.combine_region_bytes <= 49200
+
+
+def test_flat_and_hierarchical_agree(orc):
+    sizes = [3000000, 777777]
+    out = {}
+    for hier in (True, False):
+        prob = Problem(4, sizes, 14, 1, True)
+        reports, _ = run_steps(orc, prob, 1, None,
+                               {"elems_per_row": 16, "hierarchical_stats": hier})
+        out[hier] = reports[0]
+    assert out[False].combine_launches == 0 and out[True].combine_launches == 1
+    a, b = out[True].sum_sq, out[False].sum_sq
+    assert abs(a - b) <= 1e-13 * a
+
+
+def test_no_clip_below_threshold(orc):
+    """Tiny gradients: the norm stays below max_grad_norm, no clipping."""
+    sizes = [4096, 1000]
+    prob = Problem(2, sizes, 15, 2, True)
+    cfg = rcc.adamw_cfg(replicas=2, max_grad_norm=MAXN)
+    grads = prob.host_grads(1, 1.0)      # scale 1: unscaled std 1e-3/sqrt(2), norm ~ 0.05
+    prob.load_grads(grads)
+    with session(2) as h:
+        rep = rcc.grad_sync_adamw(h, prob.sets, cfg, rcc.optim_state(scale=1.0))
+        torch.cuda.synchronize()
+    assert rep.grad_norm < MAXN and rep.clip_coef == 1.0 and rep.skipped == 0
+    sc = orc.scaler_new(1.0)
+    orc.grad_sync_adamw_step(grads, prob.hp, prob.hm, prob.hv, lr=LR, beta1=B1, beta2=B2,
+                             eps=EPS, weight_decay=WD, max_grad_norm=MAXN, step=0, scaler=sc)
+    for i in range(len(sizes)):
+        assert close(to_host(prob.tensors[i]["params"][1]), prob.hp[i])
+
+
+def test_descriptor_cache_follows_pointer_changes(orc):
+    """Re-running with different gradient buffers (new pointers) must use them."""
+    sizes = [10000, 2000]
+    prob = Problem(2, sizes, 16, 1, True)
+    run_steps(orc, prob, 2, None, {})
+    # swap in fresh gradient tensors: the descriptor must be re-uploaded
+    for t in prob.tensors:
+        t["grads"] = [torch.empty_like(g) for g in t["grads"]]
+    prob.sets = rcc.ParamSets(prob.tensors)
+    run_steps(orc, prob, 1, None, {})
+
+
+def test_full_1024_tensors_ten_steps(orc):
+    """1024 fp32 tensors, sizes log-uniform in [1024, 4194304], R = 4, grads
+    N(0, 1e-3) x 65536, 10 steps, NaN at step 7.  The oracle runs streamed per
+    tensor on host copies of the same device-generated gradients."""
+    R, P = 4, 1024
+    sizes = synth.param_sizes(P, 1024, 4194304, 20)
+    rep_count = 4
+    p_dev, m_dev, v_dev, g_dev, mg_dev = [], [], [], [], []
+    hp, hm, hv = [], [], []
+    for i, n in enumerate(sizes):
+        p0 = synth.gpu_draw("normal:0.02", n, torch.float32, (21, i), DEV)
+        p_dev.append([p0.clone() for _ in range(rep_count)])
+        m_dev.append([torch.zeros(n, device=DEV) for _ in range(rep_count)])
+        v_dev.append([torch.zeros(n, device=DEV) for _ in range(rep_count)])
+        g_dev.append([torch.empty(n, device=DEV) for _ in range(R)])
+        mg_dev.append(torch.empty(n, device=DEV))
+        hp.append(to_host(p0))
+        hm.append(np.zeros(n, np.float32))
+        hv.append(np.zeros(n, np.float32))
+    sets = rcc.ParamSets([dict(grads=g_dev[i], params=p_dev[i], exp_avg=m_dev[i],
+                               exp_avg_sq=v_dev[i], mean_grad=mg_dev[i]) for i in range(P)])
+    cfg = rcc.adamw_cfg(lr=LR, betas=(B1, B2), eps=EPS, weight_decay=WD, max_grad_norm=MAXN,
+                        replicas=rep_count)
+    state = rcc.optim_state(scale=65536.0)
+    sc = orc.scaler_new(65536.0)
+    t = 0
+    with session(R) as h:
+        for k in range(1, 11):
+            for i, n in enumerate(sizes):
+                for r in range(R):
+                    g_dev[i][r].copy_(synth.gpu_draw("normal:1e-3", n, torch.float32,
+                                                     (22, i, k, r), DEV) * state.scale)
+            if k == 7:
+                g_dev[0][0][0] = float("nan")
+            rep = rcc.grad_sync_adamw(h, sets, cfg, state)
+            torch.cuda.synchronize()
+            # oracle, streamed per tensor
+            inv = np.float32(1.0 / sc.scale)
+            st = orc.stats_new()
+            means = []
+            for i in range(P):
+                mean = orc.mean_unscale([to_host(g) for g in g_dev[i]], inv)
+                orc.stats_accumulate(st, mean)
+                means.append(mean)
+            d = orc.decide(st, MAXN)
+            assert rep.skipped == d.skip and rep.nonfinite == st.nonfinite
+            if d.skip:
+                orc.scaler_update(sc, True)
+            else:
+                want = orc.stats_value(st)
+                assert abs(rep.sum_sq - want) <= 1e-12 * want
+                t += 1
+                s = orc.adamw_scalars(LR, B1, B2, EPS, WD, t)
+                for i in range(P):
+                    orc.adamw_update(means[i], d.clip_coef, s, hp[i], hm[i], hv[i])
+                orc.scaler_update(sc, False)
+            assert state.step == t and state.scale == sc.scale
+            assert rep.combine_launches == _levels(rep.stats_rows)
+    assert t == 9 and state.scale == 32768.0
+    bad = 0
+    for i in range(P):
+        if not close(to_host(p_dev[i][0]), hp[i]):
+            bad += 1
+        for j in range(1, rep_count):
+            assert torch.equal(p_dev[i][j], p_dev[i][0])
+    assert bad == 0
+    assert math.isfinite(rep.grad_norm)
