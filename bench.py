@@ -63,6 +63,16 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="step",
+                    choices=["step", "all_reduce", "reduce", "broadcast", "reduce_scatter",
+                             "all_gather", "grad_sync"],
+                    help="step: the whole hot path (the benchmark line); otherwise time one "
+                         "collective alone on --ranks x --elems (profiling and sweeps)")
+    ap.add_argument("--ranks", type=int, default=R)
+    ap.add_argument("--elems", type=int, default=N)
+    ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--op", default="sum", choices=["sum", "mean", "max", "min"])
+    ap.add_argument("--fast", action="store_true", help="pairwise-tree sums instead of rank order")
     return ap.parse_args()
 
 
@@ -440,8 +450,82 @@ def bench_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def bench_case(args):
+    """One collective alone, timed with CUDA events; prints one JSON line."""
+    import torch
+    from gradient_sync_rcc_gb300 import build, rcc, synth
+    build.build()
+    dev = "cuda:0"
+    Rk, n = args.ranks, args.elems
+    dt = rcc.F32 if args.dtype == "f32" else rcc.BF16
+    td = torch.float32 if dt == rcc.F32 else torch.bfloat16
+    es = 4 if dt == rcc.F32 else 2
+    c = args.case
+    n_in = n // Rk if c == "all_gather" else n
+    ins = synth.gpu_rank_buffers("uniform", Rk, n_in, td, (3, Rk, n), dev)
+    if c == "reduce_scatter":
+        outs = [torch.empty(n // Rk, dtype=td, device=dev) for _ in range(Rk)]
+    elif c == "reduce":
+        outs = torch.empty(n, dtype=td, device=dev)
+    else:
+        outs = [torch.empty(n, dtype=td, device=dev) for _ in range(Rk)]
+    traffic = {"all_reduce": 2 * Rk * n * es, "reduce": (Rk + 1) * n * es,
+               "broadcast": (Rk + 1) * n * es, "reduce_scatter": (Rk * n + n) * es,
+               "all_gather": (n + Rk * n) * es}.get(c)
+    h = rcc.register(0, Rk, dt, not args.fast)
+    sets = None
+    if c == "grad_sync":
+        p0 = synth.gpu_draw("normal:0.02", n, torch.float32, (3, 9), dev)
+        sets = rcc.ParamSets([dict(grads=ins, params=[p0], exp_avg=[torch.zeros_like(p0)],
+                                   exp_avg_sq=[torch.zeros_like(p0)],
+                                   mean_grad=torch.empty_like(p0))])
+        cfg, state = rcc.adamw_cfg(replicas=1), rcc.optim_state(scale=1.0)
+        traffic = (Rk * 4 + 4) * n + 28 * n
+
+    def once():
+        if c == "all_reduce":
+            rcc.all_reduce(h, ins, outs, args.op)
+        elif c == "reduce":
+            rcc.reduce(h, ins, outs, root=Rk - 1, op=args.op)
+        elif c == "broadcast":
+            rcc.broadcast(h, ins[0], outs, root=0)
+        elif c == "reduce_scatter":
+            rcc.reduce_scatter(h, ins, outs, args.op)
+        elif c == "all_gather":
+            rcc.all_gather(h, ins, outs)
+        else:
+            rcc.grad_sync_adamw(h, sets, cfg, state)
+
+    try:
+        for _ in range(max(args.warmup, 3)):
+            once()
+        torch.cuda.synchronize()
+        K = args.steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        ev[0].record()
+        for k in range(K):
+            once()
+            ev[k + 1].record()
+        torch.cuda.synchronize()
+        ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+    finally:
+        rcc.finish(h)
+    peak, src = peak_hbm()
+    med = statistics.median(ms)
+    print(json.dumps({"case": c, "ranks": Rk, "elems": n, "dtype": args.dtype, "op": args.op,
+                      "mode": "fast" if args.fast else "deterministic",
+                      "median_ms": round(med, 5), "min_ms": round(min(ms), 5),
+                      "algbw_gbs": round(Rk * n * es / (med * 1e-3) / 1e9, 1),
+                      "traffic_gbs": round(traffic / (med * 1e-3) / 1e9, 1),
+                      "frac_of_" + src: round(traffic / (med * 1e-3) / 1e9 / peak, 4),
+                      "min_traffic_bytes": traffic}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.case != "step":
+        bench_case(args)
+        return
     if args.impl == "reference":
         bench_reference(args)
     else:

@@ -129,7 +129,9 @@ def test_reduce_scatter_all_gather_8_ranks_2p26_bf16(orc, det):
         assert bits_equal(got, want)
     ok, loose = within_one_bf16_ulp(orc, got, xs, "sum")
     assert ok
-    assert loose < 64, loose      # heavy-cancellation elements are rare
+    # elements held to the accumulation bound instead of one ulp: the few
+    # whose sum cancels to |y| below ~R 2^-16 sum|x| (about 1e-4 of N(0,1) data)
+    assert loose < 1e-3 * N, loose
 
 
 # ---------------------------------------------------------------- size sweep
