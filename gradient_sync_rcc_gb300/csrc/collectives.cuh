@@ -18,6 +18,7 @@
 
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <unordered_map>
 
@@ -29,23 +30,56 @@ namespace mp {
 constexpr uint32_t kCanonicalNaN = 0x7FC00000u;
 
 // ---- memory access -------------------------------------------------------
-// Streaming 16-byte load through the non-coherent path without L1
-// allocation: every input element is read exactly once.  Volatile keeps the
-// loads and stores of one thread in program order (in-place all_reduce reads
-// an element before the same thread overwrites it).
-__device__ __forceinline__ uint4 ld_vec(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+// A vector of W 32-bit words: W = 4 (16 bytes) or W = 8 (32 bytes, the
+// 256-bit global loads/stores sm_100-class GPUs provide).
+template <int W>
+struct Vec {
+  uint32_t w[W];
+};
+
+// Streaming load through the non-coherent path without L1 allocation: every
+// input element is read exactly once.  Volatile keeps the loads and stores of
+// one thread in program order (in-place all_reduce reads an element before the
+// same thread overwrites it).
+template <int W>
+__device__ __forceinline__ Vec<W> ld_vec(const void* p) {
+  Vec<W> v;
+  if constexpr (W == 4) {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+  }
   return v;
 }
 
-// Streaming (evict-first) 16-byte store: outputs are not re-read by this pass.
-__device__ __forceinline__ void st_vec(void* p, const uint4& v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
+// Output stores.  RCC_STORE_HINT 1 marks them streaming (evict-first): this
+// pass never re-reads what it writes.  0 uses the default write-back policy.
+#ifndef RCC_STORE_HINT
+#define RCC_STORE_HINT 1
+#endif
+#if RCC_STORE_HINT
+#define RCC_ST "st.global.cs"
+#else
+#define RCC_ST "st.global"
+#endif
+
+template <int W>
+__device__ __forceinline__ void st_vec(void* p, const Vec<W>& v) {
+  if constexpr (W == 4) {
+    asm volatile(RCC_ST ".v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                 "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+  } else {
+    asm volatile(RCC_ST ".v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+                 "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+                 "r"(v.w[7])
+                 : "memory");
+  }
 }
 
 // ---- element types ---------------------------------------------------------
@@ -69,17 +103,19 @@ struct Elem;
 
 template <>
 struct Elem<float> {
-  static constexpr int kPerVec = 4;
   static constexpr int kBytes = 4;
-  __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
-    f[0] = __uint_as_float(v.x);
-    f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z);
-    f[3] = __uint_as_float(v.w);
+  static constexpr int kPerWord = 1;
+  template <int W>
+  __device__ static __forceinline__ void unpack(const Vec<W>& v, float* f) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) f[k] = __uint_as_float(v.w[k]);
   }
-  __device__ static __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
-                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  template <int W>
+  __device__ static __forceinline__ Vec<W> pack(const float* f) {
+    Vec<W> v;
+#pragma unroll
+    for (int k = 0; k < W; ++k) v.w[k] = __float_as_uint(f[k]);
+    return v;
   }
   __device__ static __forceinline__ float load(const void* p, size_t i) {
     return static_cast<const float*>(p)[i];
@@ -94,19 +130,22 @@ struct Elem<float> {
 
 template <>
 struct Elem<__nv_bfloat16> {
-  static constexpr int kPerVec = 8;
   static constexpr int kBytes = 2;
-  __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  static constexpr int kPerWord = 2;
+  template <int W>
+  __device__ static __forceinline__ void unpack(const Vec<W>& v, float* f) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      f[2 * k] = __uint_as_float(w[k] << 16);
-      f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    for (int k = 0; k < W; ++k) {
+      f[2 * k] = __uint_as_float(v.w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(v.w[k] & 0xFFFF0000u);
     }
   }
-  __device__ static __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(bf16x2_rn(f[0], f[1]), bf16x2_rn(f[2], f[3]),
-                      bf16x2_rn(f[4], f[5]), bf16x2_rn(f[6], f[7]));
+  template <int W>
+  __device__ static __forceinline__ Vec<W> pack(const float* f) {
+    Vec<W> v;
+#pragma unroll
+    for (int k = 0; k < W; ++k) v.w[k] = bf16x2_rn(f[2 * k], f[2 * k + 1]);
+    return v;
   }
   __device__ static __forceinline__ float load(const void* p, size_t i) {
     return __uint_as_float((uint32_t)static_cast<const uint16_t*>(p)[i] << 16);
@@ -202,17 +241,19 @@ struct SegView {
 
 // NS > 0: compile-time number of sources (U vectors per thread in flight per
 // source); NS == 0: runtime count (any R up to kMaxRanks), sources loaded in
-// groups of 8 and folded in rank order.
-template <typename T, int NS, int RED, bool FAST, int U>
+// groups of 8 and folded in rank order.  W: 32-bit words per vector (4 or 8);
+// the host picks 8 only when every address is 32-byte aligned.
+template <typename T, int NS, int RED, bool FAST, int U, int W>
 __global__ void __launch_bounds__(kThreads)
     mp_kernel(const __grid_constant__ MultiPtrArgs a) {
   using E = Elem<T>;
-  constexpr int EPV = E::kPerVec;
+  constexpr int EPV = W * E::kPerWord;  // elements per vector
+  constexpr int VB = 4 * W;             // bytes per vector
   constexpr int EB = E::kBytes;
   const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
                    (size_t)blockIdx.y * a.dst_seg_stride};
   const int ndst = sv.ndst();
-  const size_t nv = a.vec_ok ? a.n / EPV : 0;
+  const size_t nv = a.vec_ok >= VB ? a.n / EPV : 0;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t nthreads = (size_t)gridDim.x * blockDim.x;
 
@@ -223,26 +264,26 @@ __global__ void __launch_bounds__(kThreads)
 
     for (size_t base = (size_t)blockIdx.x * blockDim.x * U + threadIdx.x; base < nv;
          base += nthreads * U) {
-      uint4 v[U][NS];
+      Vec<W> v[U][NS];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const size_t idx = base + (size_t)u * blockDim.x;
         if (idx < nv) {
 #pragma unroll
-          for (int q = 0; q < NS; ++q) v[u][q] = ld_vec(sp[q] + idx * 16);
+          for (int q = 0; q < NS; ++q) v[u][q] = ld_vec<W>(sp[q] + idx * VB);
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const size_t idx = base + (size_t)u * blockDim.x;
         if (idx < nv) {
-          uint4 out;
+          Vec<W> out;
           if constexpr (RED == kRedCopy) {
             out = v[u][0];
           } else {
             float f[NS][EPV];
 #pragma unroll
-            for (int q = 0; q < NS; ++q) E::unpack(v[u][q], f[q]);
+            for (int q = 0; q < NS; ++q) E::template unpack<W>(v[u][q], f[q]);
             float r[EPV];
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
@@ -251,10 +292,10 @@ __global__ void __launch_bounds__(kThreads)
               for (int q = 0; q < NS; ++q) x[q] = f[q][e];
               r[e] = reduce_lane<NS, RED, FAST>(x, a.mean_div);
             }
-            out = E::pack(r);
+            out = E::template pack<W>(r);
           }
           for (int d = 0; d < ndst; ++d)
-            st_vec(static_cast<char*>(sv.dst(d, EB)) + idx * 16, out);
+            st_vec<W>(static_cast<char*>(sv.dst(d, EB)) + idx * VB, out);
         }
       }
     }
@@ -264,15 +305,16 @@ __global__ void __launch_bounds__(kThreads)
     for (size_t idx = tid; idx < nv; idx += nthreads) {
       Acc<RED> acc[EPV];
       for (int q0 = 0; q0 < R; q0 += 8) {
-        uint4 v[8];
+        Vec<W> v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          if (q0 + k < R) v[k] = ld_vec(static_cast<const char*>(sv.src(q0 + k, EB)) + idx * 16);
+          if (q0 + k < R)
+            v[k] = ld_vec<W>(static_cast<const char*>(sv.src(q0 + k, EB)) + idx * VB);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           if (q0 + k < R) {
             float f[EPV];
-            E::unpack(v[k], f);
+            E::template unpack<W>(v[k], f);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
               if (q0 + k == 0)
@@ -286,9 +328,9 @@ __global__ void __launch_bounds__(kThreads)
       float r[EPV];
 #pragma unroll
       for (int e = 0; e < EPV; ++e) r[e] = acc[e].result(a.mean_div);
-      const uint4 out = E::pack(r);
+      const Vec<W> out = E::template pack<W>(r);
       for (int d = 0; d < ndst; ++d)
-        st_vec(static_cast<char*>(sv.dst(d, EB)) + idx * 16, out);
+        st_vec<W>(static_cast<char*>(sv.dst(d, EB)) + idx * VB, out);
     }
   }
 
@@ -316,8 +358,9 @@ __global__ void __launch_bounds__(kThreads)
 
 // ---- host-side dispatch -------------------------------------------------------
 
-// Vectors per thread in flight for each source count: enough 16-byte loads
-// outstanding per thread (U * NS >= 4..8) to cover HBM latency.
+// 16-byte vectors per thread in flight for each source count: enough loads
+// outstanding per thread (U * NS >= 4..8) to cover HBM latency.  32-byte
+// vectors halve U.
 constexpr int unroll_for(int ns, int red) {
   return red == kRedCopy ? 4 : ns <= 2 ? 4 : ns <= 4 ? 2 : 1;
 }
@@ -349,12 +392,22 @@ inline int resident_blocks(const void* fn) {
   return per_sm;
 }
 
-template <typename T, int NS, int RED, bool FAST>
-cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  constexpr int U = NS > 0 ? unroll_for(NS, RED) : 1;
-  constexpr int EPV = Elem<T>::kPerVec;
-  auto fn = mp_kernel<T, NS, RED, FAST, U>;
-  const size_t nv = a.vec_ok ? a.n / EPV : 0;
+// Widest vector the addresses allow (RCC_VEC_BYTES=16 caps it at 16 bytes).
+inline int vec_cap() {
+  static int cap = [] {
+    const char* v = std::getenv("RCC_VEC_BYTES");
+    return (v && std::atoi(v) == 16) ? 16 : 32;
+  }();
+  return cap;
+}
+
+template <typename T, int NS, int RED, bool FAST, int W>
+cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+  constexpr int U0 = NS > 0 ? unroll_for(NS, RED) * 4 / W : 1;
+  constexpr int U = U0 > 0 ? U0 : 1;
+  constexpr int EPV = W * Elem<T>::kPerWord;
+  auto fn = mp_kernel<T, NS, RED, FAST, U, W>;
+  const size_t nv = a.vec_ok >= 4 * W ? a.n / EPV : 0;
   const size_t tail = a.n - nv * EPV;
   size_t want = (nv + (size_t)kThreads * U - 1) / ((size_t)kThreads * U);
   const size_t want_tail = (tail + kThreads - 1) / kThreads;
@@ -366,6 +419,12 @@ cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   const unsigned gx = (unsigned)(want < cap ? want : cap);
   fn<<<dim3(gx, (unsigned)nseg), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <typename T, int NS, int RED, bool FAST>
+cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+  if (a.vec_ok >= 32 && vec_cap() >= 32) return launch_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+  return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
 }
 
 template <typename T, int RED, bool FAST>

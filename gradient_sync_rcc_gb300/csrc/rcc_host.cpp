@@ -234,16 +234,16 @@ rcc_status launch(const Session& s, rcc::Red red, int nseg, const MultiPtrArgs& 
   return RCC_OK;
 }
 
-// 16-byte vectors are usable when every base address is 16-byte aligned and
-// every per-segment offset keeps it so.
+// The widest vector (32 or 16 bytes, else 0) that every base address and
+// every per-segment offset is a multiple of.
 int vec_ok(const MultiPtrArgs& a, int nsrc_ptrs, int ndst_ptrs, size_t seg_bytes_src,
            size_t seg_bytes_dst) {
-  for (int i = 0; i < nsrc_ptrs; ++i)
-    if (!aligned16(a.src[i])) return 0;
-  for (int i = 0; i < ndst_ptrs; ++i)
-    if (!aligned16(a.dst[i])) return 0;
-  if (seg_bytes_src % 16 || seg_bytes_dst % 16) return 0;
-  return 1;
+  uintptr_t bits = seg_bytes_src | seg_bytes_dst;
+  for (int i = 0; i < nsrc_ptrs; ++i) bits |= reinterpret_cast<uintptr_t>(a.src[i]);
+  for (int i = 0; i < ndst_ptrs; ++i) bits |= reinterpret_cast<uintptr_t>(a.dst[i]);
+  if ((bits & 31u) == 0) return 32;
+  if ((bits & 15u) == 0) return 16;
+  return 0;
 }
 
 }  // namespace

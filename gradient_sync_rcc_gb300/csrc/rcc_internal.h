@@ -37,8 +37,9 @@ struct MultiPtrArgs {
   int src_per_seg;
   int dst_per_seg;
   int mean_div;  // > 0: the sum is divided by this (IEEE division) before storing
-  int vec_ok;    // 1: every source/destination address (with segment offsets)
-                 //    is 16-byte aligned, so whole 16-byte vectors may be used
+  int vec_ok;    // alignment class in bytes (0, 16 or 32): every source and
+                 // destination address, with segment offsets, is a multiple of
+                 // it, so vectors of that many bytes may be used
 };
 
 // One launch of the pass; fast selects the pairwise-tree sum.

@@ -13,7 +13,9 @@ import ctypes as C
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "librcc.so")
+# RCC_LIBRARY may name another build of the same library (e.g. one compiled
+# with different tuning macros); there is no fallback either way.
+LIB_PATH = os.environ.get("RCC_LIBRARY") or os.path.join(HERE, "librcc.so")
 
 # status codes, dtypes, ops, flags (mirrors include/rcc.h)
 OK = 0

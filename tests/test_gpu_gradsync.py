@@ -74,8 +74,8 @@ class Problem:
                 self.tensors[i]["grads"][r].copy_(to_dev(per[r]))
 
 
-def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0):
-    cfg = rcc.adamw_cfg(lr=LR, betas=(B1, B2), eps=EPS, weight_decay=WD, max_grad_norm=MAXN,
+def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, max_norm=MAXN):
+    cfg = rcc.adamw_cfg(lr=LR, betas=(B1, B2), eps=EPS, weight_decay=WD, max_grad_norm=max_norm,
                         replicas=prob.rep, **cfg_kw)
     state = rcc.optim_state(scale=scale)
     sc = orc.scaler_new(scale)
@@ -90,7 +90,7 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0):
             torch.cuda.synchronize()
             ostep, st, d = orc.grad_sync_adamw_step(
                 grads, prob.hp, prob.hm, prob.hv, lr=LR, beta1=B1, beta2=B2, eps=EPS,
-                weight_decay=WD, max_grad_norm=MAXN, step=ostep, scaler=sc)
+                weight_decay=WD, max_grad_norm=max_norm, step=ostep, scaler=sc)
             reports.append(rep)
             assert rep.skipped == d.skip
             assert rep.nonfinite == st.nonfinite
@@ -120,7 +120,9 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0):
 def test_ten_steps_nan_at_seven(orc, replicas, mean_grad):
     sizes = synth.param_sizes(16, 1024, 65536, 10)
     prob = Problem(4, sizes, 11, replicas, mean_grad)
-    reports, state = run_steps(orc, prob, 10, 7, {})
+    # the unscaled mean gradient has norm ~0.2 here: max_grad_norm 0.1 keeps
+    # the clip active on every applied step
+    reports, state = run_steps(orc, prob, 10, 7, {}, max_norm=0.1)
     assert [r.skipped for r in reports] == [0] * 6 + [1] + [0] * 3
     assert state.step == 9 and state.scale == 32768.0
     assert all(r.combine_launches == 0 for r in reports)      # <= 1024 rows
