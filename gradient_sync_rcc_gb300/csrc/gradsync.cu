@@ -23,6 +23,10 @@
 // Row layout: three u32 words {low, high word of the fp64 sum, count}.
 #include <cuda_runtime.h>
 
+#include <cmath>
+#include <mutex>
+
+#include "rcc.h"
 #include "rcc_internal.h"
 
 namespace rcc {
@@ -369,4 +373,184 @@ cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---- statistics without allocation -----------------------------------------
+// For callers that cannot allocate device memory at all: code running inside a
+// CUDA-graph capture that forbids cudaMalloc, processes whose memory is owned
+// by another runtime or pool, or integrations that may only pass their own
+// buffers.  The statistics rows of one call live in this file-scope device
+// array instead of session scratch.  Every GPU that loads the library holds it
+// (196,800 bytes) until the process exits.  Host code may not use the array's
+// name as a device address: rcc_grad_stats_noalloc looks the address up once
+// per device with cudaGetSymbolAddress and passes it to the kernels.
+
+namespace gs {
+
+constexpr uint64_t kNoAllocMaxRows = 16384;
+constexpr uint32_t kNoAllocElemsPerRow = 8192;
+constexpr uint64_t kNoAllocMaxElems = kNoAllocMaxRows * kNoAllocElemsPerRow;
+// statistics rows, then the <= 16 rows of the single combine level
+static __device__ __align__(256) uint32_t g_noalloc_rows[(kNoAllocMaxRows + 16) * 3];
+
+struct OneTensorArgs {
+  const float* grads[kMaxRanks];  // R device pointers, passed by value
+  float* mean_grad;
+  uint32_t* rows;                 // device address of g_noalloc_rows
+  uint64_t numel;
+  int R;
+  int vec_ok;
+  float inv_scale;
+};
+
+// gs_stats_kernel for a single tensor whose R gradient pointers arrive in the
+// launch arguments (no device pointer table, hence nothing to upload).
+template <int RC>
+__global__ void __launch_bounds__(kThreads)
+    gs_stats_one_kernel(const __grid_constant__ OneTensorArgs a) {
+  const uint64_t row = blockIdx.x;
+  const int R = RC > 0 ? RC : a.R;
+  const float* const* g = a.grads;
+  const uint64_t c0 = row * (uint64_t)kNoAllocElemsPerRow;
+  uint64_t c1 = c0 + kNoAllocElemsPerRow;
+  if (c1 > a.numel) c1 = a.numel;
+
+  SqAcc acc;
+  uint64_t scalar_from = c0;
+  if (a.vec_ok) {
+    const uint64_t v0 = c0 / 4, v1 = c1 / 4;
+    scalar_from = v1 * 4;
+    for (uint64_t v = v0 + threadIdx.x; v < v1; v += 2 * kThreads) {
+      uint4 x[2][RC > 0 ? RC : 1];
+      if constexpr (RC > 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint64_t vi = v + (uint64_t)u * kThreads;
+          if (vi < v1) {
+#pragma unroll
+            for (int q = 0; q < RC; ++q) x[u][q] = ld_vec(g[q] + vi * 4);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint64_t vi = v + (uint64_t)u * kThreads;
+        if (vi >= v1) continue;
+        float m[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (RC > 0) {
+            float col[RC];
+#pragma unroll
+            for (int q = 0; q < RC; ++q)
+              col[q] = __uint_as_float(e == 0 ? x[u][q].x : e == 1 ? x[u][q].y
+                                        : e == 2 ? x[u][q].z : x[u][q].w);
+            m[e] = mean_unscale(col, RC, a.inv_scale);
+          } else {
+            float s = g[0][vi * 4 + e];
+            for (int q = 1; q < R; ++q) s = __fadd_rn(s, g[q][vi * 4 + e]);
+            m[e] = __fmul_rn(__fdiv_rn(s, (float)R), a.inv_scale);
+          }
+          acc.add(m[e]);
+        }
+        if (a.mean_grad)
+          st_vec(a.mean_grad + vi * 4, make_uint4(__float_as_uint(m[0]), __float_as_uint(m[1]),
+                                                  __float_as_uint(m[2]), __float_as_uint(m[3])));
+      }
+    }
+  }
+  for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads) {
+    float s = g[0][i];
+    for (int q = 1; q < R; ++q) s = __fadd_rn(s, g[q][i]);
+    const float m = __fmul_rn(__fdiv_rn(s, (float)R), a.inv_scale);
+    acc.add(m);
+    if (a.mean_grad) a.mean_grad[i] = m;
+  }
+  block_reduce_row(acc.value(), acc.nonfinite, a.rows + row * 3);
+}
+
+}  // namespace gs
+
+namespace {
+
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_dev_ptr[256] = {};  // per device ordinal, set on first use
+
+bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
 }  // namespace rcc
+
+extern "C" rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_ranks,
+                                             size_t numel, double loss_scale,
+                                             float* mean_grad, uint32_t* report,
+                                             rcc_stream_t stream) {
+  using namespace rcc;
+  if (!grads || !report)
+    return set_error(RCC_ERR_INVALID_ARGUMENT, "grads and report are required");
+  if (num_ranks < 1 || num_ranks > kMaxRanks)
+    return set_error(RCC_ERR_INVALID_ARGUMENT, "num_ranks outside [1, 64]");
+  for (int r = 0; r < num_ranks; ++r)
+    if (!grads[r]) return set_error(RCC_ERR_MISSING_REGISTRATION, "a rank supplies no gradient");
+  if (numel == 0 || numel > gs::kNoAllocMaxElems)
+    return set_error(RCC_ERR_INVALID_ARGUMENT,
+                     "numel must be in [1, 134217728] (16384 rows of 8192 elements, the "
+                     "size of the static statistics array)");
+  if (!(std::isfinite(loss_scale) && loss_scale > 0.0))
+    return set_error(RCC_ERR_INVALID_ARGUMENT, "loss_scale must be finite and > 0");
+  if (reinterpret_cast<uintptr_t>(report) & 3u)
+    return set_error(RCC_ERR_INVALID_ARGUMENT, "report must be 4-byte aligned");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
+  if (dev < 0 || dev >= 256) return set_error(RCC_ERR_INVALID_ARGUMENT, "device ordinal >= 256");
+  uint32_t* rows = nullptr;
+  {
+    // set-up, once per device, with that device current: the host-side name
+    // of the array is not a device address, so fetch the real one
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_dev_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, gs::g_noalloc_rows);
+      if (e != cudaSuccess) return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
+      g_noalloc_dev_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    rows = g_noalloc_dev_ptr[dev];
+  }
+  gs::OneTensorArgs a{};
+  bool vec = mean_grad == nullptr || aligned16_ptr(mean_grad);
+  for (int r = 0; r < num_ranks; ++r) {
+    a.grads[r] = grads[r];
+    vec = vec && aligned16_ptr(grads[r]);
+  }
+  a.mean_grad = mean_grad;
+  a.rows = rows;
+  a.numel = numel;
+  a.R = num_ranks;
+  a.vec_ok = vec ? 1 : 0;
+  a.inv_scale = (float)(1.0 / loss_scale);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const uint64_t nrows = (numel + gs::kNoAllocElemsPerRow - 1) / gs::kNoAllocElemsPerRow;
+  const dim3 grid((unsigned)nrows);
+  switch (num_ranks) {
+    case 1: gs::gs_stats_one_kernel<1><<<grid, kThreads, 0, cs>>>(a); break;
+    case 2: gs::gs_stats_one_kernel<2><<<grid, kThreads, 0, cs>>>(a); break;
+    case 4: gs::gs_stats_one_kernel<4><<<grid, kThreads, 0, cs>>>(a); break;
+    case 8: gs::gs_stats_one_kernel<8><<<grid, kThreads, 0, cs>>>(a); break;
+    default: gs::gs_stats_one_kernel<0><<<grid, kThreads, 0, cs>>>(a); break;
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
+  uint64_t launched = 1;
+  const uint32_t* src = rows;
+  uint64_t n = nrows;
+  if (n > (uint64_t)gs::kFanIn) {
+    uint32_t* out = rows + gs::kNoAllocMaxRows * 3;
+    if ((e = launch_gs_combine(src, n, out, cs)) != cudaSuccess)
+      return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
+    src = out;
+    n = (n + gs::kFanIn - 1) / gs::kFanIn;
+    ++launched;
+  }
+  if ((e = launch_gs_report(src, n, report, cs)) != cudaSuccess)
+    return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
+  add_launches(launched + 1);
+  return RCC_OK;
+}

@@ -248,6 +248,11 @@ int vec_ok(const MultiPtrArgs& a, int nsrc_ptrs, int ndst_ptrs, size_t seg_bytes
 
 }  // namespace
 
+namespace rcc {
+rcc_status set_error(rcc_status st, const char* msg) { return fail(st, "%s", msg); }
+void add_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace rcc
+
 // ============================================================================
 extern "C" {
 

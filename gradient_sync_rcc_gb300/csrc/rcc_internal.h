@@ -7,6 +7,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "rcc.h"
+
 namespace rcc {
 
 constexpr int kMaxRanks = 64;
@@ -101,5 +103,10 @@ struct GsUpdateArgs {
 };
 
 cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream);
+
+// Host layer services for entry points defined outside rcc_host.cpp: record
+// the calling thread's error text (returns st), count kernel launches.
+rcc_status set_error(rcc_status st, const char* msg);
+void add_launches(uint64_t n);
 
 }  // namespace rcc

@@ -37,8 +37,8 @@ MAX_RANKS = 64
 # every symbol include/rcc.h declares
 SYMBOLS = ["rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
            "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
-           "rcc_grad_sync_adamw", "rcc_last_error_message", "rcc_status_string",
-           "rcc_kernel_launch_count"]
+           "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc", "rcc_last_error_message",
+           "rcc_status_string", "rcc_kernel_launch_count"]
 
 
 class ParamSet(C.Structure):
@@ -97,9 +97,11 @@ def lib():
         L.rcc_grad_sync_adamw.argtypes = [C.c_void_p, C.POINTER(ParamSet), C.c_int,
                                           C.POINTER(AdamWCfg), C.POINTER(OptimState),
                                           C.POINTER(StepReport), C.c_void_p]
+        L.rcc_grad_stats_noalloc.argtypes = [_PP, C.c_int, C.c_size_t, C.c_double, C.c_void_p,
+                                             C.c_void_p, C.c_void_p]
         for name in ("rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
                      "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
-                     "rcc_grad_sync_adamw"):
+                     "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc"):
             getattr(L, name).restype = st
         L.rcc_last_error_message.restype = C.c_char_p
         L.rcc_last_error_message.argtypes = []
@@ -271,6 +273,14 @@ def grad_sync_adamw(comm, param_sets, cfg, state, stream=None):
     _check(lib().rcc_grad_sync_adamw(comm, param_sets.arr, len(param_sets), C.byref(cfg),
                                      C.byref(state), C.byref(rep), _stream(stream)))
     return rep
+
+
+def grad_stats_noalloc(grads, loss_scale, report, mean_grad=None, stream=None):
+    """rcc_grad_stats_noalloc for one tensor: grads are R device tensors,
+    report a device tensor of at least 12 bytes (e.g. torch.int32 x 3)."""
+    _check(lib().rcc_grad_stats_noalloc(ptr_array([g.data_ptr() for g in grads]), len(grads),
+                                        grads[0].numel(), float(loss_scale), _ptr(mean_grad),
+                                        report.data_ptr(), _stream(stream)))
 
 
 # ------------------------------------------------------------- raw calls (status only)

@@ -232,6 +232,41 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params,
                                rcc_optim_state* state, rcc_step_report* report,
                                rcc_stream_t stream);
 
+/* ---- gradient statistics without allocation ------------------------------- */
+
+/* The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory at all -- code running while a stream is
+ * being captured into a CUDA graph with allocation forbidden, processes whose
+ * device memory belongs to another runtime or a fixed pool, or hosts that may
+ * only pass buffers they already own.  rcc_grad_sync_adamw allocates session
+ * scratch on first use; this call never does (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *
+ * It computes steps 1-2 of rcc_grad_sync_adamw for ONE parameter tensor:
+ * g = fl32(fl32(sum_q grads[q]) / R) * fl32(1 / loss_scale), optionally
+ * stored to mean_grad[numel] (device, may be NULL), and writes the 12-byte
+ * report {low word, high word of the fp64 sum of g^2 over finite g, u32 count
+ * of non-finite g} to `report` (device, 4-byte aligned).  Rows of 8192
+ * elements and the fan-in-1024 combine are the same as rcc_grad_sync_adamw's
+ * with its default elems_per_row, so the two give the same report.
+ *
+ * Limits and behaviour:
+ *   - grads: host array of num_ranks (1..RCC_MAX_RANKS) device pointers;
+ *     numel in [1, 134,217,728] (16,384 rows); anything larger returns
+ *     RCC_ERR_INVALID_ARGUMENT.
+ *   - The rows live in one file-scope device array of 196,800 bytes that every
+ *     GPU which loads the library keeps until the process exits.  All calls
+ *     share it: calls that overlap on the GPU (different streams, no ordering)
+ *     race on it.  Every row is rewritten before it is read, so nothing needs
+ *     clearing between calls.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Asynchronous on `stream`; no session is needed. */
+rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_ranks,
+                                  size_t numel, double loss_scale,
+                                  float* mean_grad, uint32_t* report,
+                                  rcc_stream_t stream);
+
 /* ---- diagnostics ---------------------------------------------------------- */
 
 /* Message describing the calling thread's most recent error ("" if none). */
