@@ -74,6 +74,7 @@ def _declare(L):
         "orc_broadcast": (C.c_int, [C.c_int, C.c_int, _P, _PP, _SZ]),
         "orc_reduce_scatter": (C.c_int, [C.c_int, C.c_int, C.c_int, _PP, _PP, _SZ]),
         "orc_all_gather": (C.c_int, [C.c_int, C.c_int, _PP, _PP, _SZ]),
+        "orc_all_to_all": (C.c_int, [C.c_int, C.c_int, _PP, _PP, _SZ]),
         "orc_mean_unscale": (None, [C.c_int, _PP, _SZ, C.c_float, _P]),
         "orc_stats_accumulate": (None, [C.POINTER(Stats), _P, _SZ]),
         "orc_stats_value": (C.c_double, [C.POINTER(Stats)]),
@@ -216,6 +217,16 @@ def all_gather(xs):
     R = len(xs)
     out = [np.empty(n * R, xs[0].dtype) for _ in xs]
     rc = lib().orc_all_gather(R, _dt(xs[0]), _ptrs(xs), _ptrs(out), n)
+    assert rc == 0
+    return out
+
+
+def all_to_all(xs):
+    xs, n = _check_ranks(xs)
+    R = len(xs)
+    assert n % R == 0
+    out = [np.empty(n, xs[0].dtype) for _ in xs]
+    rc = lib().orc_all_to_all(R, _dt(xs[0]), _ptrs(xs), _ptrs(out), n)
     assert rc == 0
     return out
 

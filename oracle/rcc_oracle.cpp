@@ -261,6 +261,22 @@ int orc_all_gather(int R, int dtype, const void* const* send,
   return 0;
 }
 
+/* all_to_all_single [Monarch: split the input, scatter the split list to
+ * all ranks, concatenate what each receives]: equal splits, so rank q's
+ * chunk r lands on rank r at position q. */
+int orc_all_to_all(int R, int dtype, const void* const* send, void* const* recv,
+                   size_t n_in) {
+  if (R < 1 || !valid_dtype(dtype)) return -1;
+  if (n_in % (size_t)R != 0) return -1;
+  const size_t shard = n_in / (size_t)R, es = elem_size(dtype);
+  for (int r = 0; r < R; ++r)
+    for (int q = 0; q < R; ++q)
+      std::memcpy(static_cast<unsigned char*>(recv[r]) + (size_t)q * shard * es,
+                  static_cast<const unsigned char*>(send[q]) + (size_t)r * shard * es,
+                  shard * es);
+  return 0;
+}
+
 /* ---- gradient sync + AdamW ---------------------------------------------- */
 
 /*

@@ -91,6 +91,11 @@ int orc_reduce_scatter(int R, int dtype, int op, const void* const* send,
 int orc_all_gather(int R, int dtype, const void* const* send,
                    void* const* recv, size_t n_shard);
 
+/* all_to_all_single with equal splits, n_in = R*n_shard per rank:
+ * recv[r][q*n_shard + j] = send[q][r*n_shard + j] for every r, q */
+int orc_all_to_all(int R, int dtype, const void* const* send, void* const* recv,
+                   size_t n_in);
+
 /* ---- gradient sync + AdamW ---------------------------------------------- */
 
 /* Running statistics of the unscaled mean gradient. */

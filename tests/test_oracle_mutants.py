@@ -42,6 +42,10 @@ MUTANTS = [
     ("all_gather writes at the receiver's slot", "static_cast<unsigned char*>(recv[r]) + (size_t)q * n_shard * es",
      "static_cast<unsigned char*>(recv[r]) + (size_t)((q + 1) % R) * n_shard * es",
      [lambda orc: pins.test_collective_identities(orc, "f32", 4)]),
+    ("all_to_all takes the receiver's chunk from the wrong place",
+     "static_cast<const unsigned char*>(send[q]) + (size_t)r * shard * es",
+     "static_cast<const unsigned char*>(send[q]) + (size_t)q * shard * es",
+     [lambda orc: pins.test_all_to_all_is_a_block_transpose(orc, 3, "f32")]),
     ("unscale dropped", "g[i] = mean * inv_scale;", "g[i] = mean;",
      [pins.test_mean_unscale_exact_on_integers]),
     ("non-finite not counted", "st->nonfinite += 1;\n      continue;", "continue;",

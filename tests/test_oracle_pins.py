@@ -298,6 +298,25 @@ def test_collective_identities(orc, dtype, R):
         assert a.tobytes() == b.tobytes()
 
 
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_to_all_is_a_block_transpose(orc, R, dtype):
+    """Monarch all_to_all_single with equal splits: viewing rank q's buffer as
+    R chunks, out[r] chunk q = in[q] chunk r, i.e. numpy's transpose of the
+    (rank, chunk) axes; applying it twice gives the input back."""
+    n = 41
+    kind = "uniform" if dtype == "f32" else "bf16_uniform"
+    xs = synth.rank_buffers(kind, R, R * n, 26, R)
+    out = orc.all_to_all(xs)
+    X = np.stack(xs).reshape(R, R, n)
+    want = np.transpose(X, (1, 0, 2)).reshape(R, R * n)
+    for r in range(R):
+        assert out[r].tobytes() == want[r].tobytes()
+    back = orc.all_to_all(out)
+    for a, b in zip(back, xs):
+        assert a.tobytes() == b.tobytes()
+
+
 def test_all_reduce_in_place(orc):
     xs = synth.rank_buffers("uniform", 4, 100, 10, 0)
     copy = [x.copy() for x in xs]
