@@ -65,7 +65,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="step",
                     choices=["step", "all_reduce", "reduce", "broadcast", "reduce_scatter",
-                             "all_gather", "grad_sync"],
+                             "all_gather", "all_to_all", "grad_sync", "grad_sync_1024"],
                     help="step: the whole hot path (the benchmark line); otherwise time one "
                          "collective alone on --ranks x --elems (profiling and sweeps)")
     ap.add_argument("--ranks", type=int, default=R)
@@ -73,6 +73,10 @@ def parse_args():
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--op", default="sum", choices=["sum", "mean", "max", "min"])
     ap.add_argument("--fast", action="store_true", help="pairwise-tree sums instead of rank order")
+    ap.add_argument("--replicas", type=int, default=1, help="optimizer-state copies (grad_sync_1024)")
+    ap.add_argument("--gs-mode", default="host", choices=["host", "device", "graph"],
+                    help="grad-sync decision: host readback (default), device kernel, or device "
+                         "kernel + captured update launches")
     return ap.parse_args()
 
 
@@ -220,31 +224,81 @@ class Workload:
         self.cfg = rcc.adamw_cfg(replicas=1, max_grad_norm=1.0)
         self.state = rcc.optim_state(scale=1.0)
 
-    def step(self, h, events=None):
+    def step(self, h, events=None, ins=None, sets=None):
+        """One pass of every row over the rank buffers `ins` (default: the
+        resident workload); `sets` is the matching gradient ParamSets."""
         rcc = self.rcc
+        ins = self.ins if ins is None else ins
+        sets = self.sets if sets is None else sets
 
         def mark(i):
             if events is not None:
                 events[i].record()
 
         mark(0)
-        rcc.all_reduce(h, self.ins, self.ar, "sum")
+        rcc.all_reduce(h, ins, self.ar, "sum")
         mark(1)
-        rcc.all_reduce(h, self.ins, self.ar, "mean")
+        rcc.all_reduce(h, ins, self.ar, "mean")
         mark(2)
-        rcc.all_reduce(h, self.ins, self.ar, "max")
+        rcc.all_reduce(h, ins, self.ar, "max")
         mark(3)
-        rcc.reduce(h, self.ins, self.red, root=R - 1, op="sum")
+        rcc.reduce(h, ins, self.red, root=R - 1, op="sum")
         mark(4)
-        rcc.broadcast(h, self.ins[0], self.bc, root=0)
+        rcc.broadcast(h, ins[0], self.bc, root=0)
         mark(5)
-        rcc.reduce_scatter(h, self.ins, self.rs, "sum")
+        rcc.reduce_scatter(h, ins, self.rs, "sum")
         mark(6)
         rcc.all_gather(h, self.rs, self.ag)
         mark(7)
-        rep = rcc.grad_sync_adamw(h, self.sets, self.cfg, self.state)
+        rep = rcc.grad_sync_adamw(h, sets, self.cfg, self.state)
         mark(8)
         return rep
+
+
+def e2e_leg(torch, rcc, wl, h, K):
+    """End to end through the public API with host buffers: every step copies
+    its R input buffers from pinned host memory and reads a result back
+    (rank 0's all_reduce output and, inside the call, the 12-byte report).
+    Inputs are double-buffered: step k+1's copies run on four copy streams
+    while step k computes.  Returns ms per step."""
+    sets_in = [wl.ins, [torch.empty_like(x) for x in wl.ins]]
+    gs_sets = [wl.sets, rcc.ParamSets([dict(wl.gs_tensors[0], grads=sets_in[1])])]
+    host_in = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(R)]
+    for x, d in zip(host_in, wl.ins):
+        x.copy_(d)
+    host_out = torch.empty(N, dtype=torch.float32, pin_memory=True)
+    main = torch.cuda.current_stream()
+    nstreams = 4
+    copy_streams = [torch.cuda.Stream() for _ in range(nstreams)]
+    copied = [[torch.cuda.Event() for _ in range(nstreams)] for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def issue_copy(k):
+        b = k % 2
+        for j, cs in enumerate(copy_streams):
+            if used[b]:
+                cs.wait_event(consumed[b])   # the step that last read buffer set b is done
+            with torch.cuda.stream(cs):
+                for i in range(j, R, nstreams):
+                    sets_in[b][i].copy_(host_in[i], non_blocking=True)
+            copied[b][j].record(cs)
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    issue_copy(0)
+    for k in range(K):
+        b = k % 2
+        if k + 1 < K:
+            issue_copy(k + 1)
+        for ev in copied[b]:
+            main.wait_event(ev)
+        wl.step(h, ins=sets_in[b], sets=gs_sets[b])
+        consumed[b].record(main)
+        used[b] = True
+        host_out.copy_(wl.ar[0], non_blocking=True)
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) * 1e3 / K
 
 
 def copy_bandwidth(torch, device):
@@ -303,20 +357,8 @@ def bench_ours(args):
 
         # end to end: inputs from pinned host memory, result read back, every step
         Ke = max(3, min(K, 20))
-        host_in = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(R)]
-        for x, d in zip(host_in, wl.ins):
-            x.copy_(d)
-        host_out = torch.empty(N, dtype=torch.float32, pin_memory=True)
-        torch.cuda.synchronize()
         barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(Ke):
-            for x, d in zip(host_in, wl.ins):
-                d.copy_(x, non_blocking=True)
-            wl.step(h)
-            host_out.copy_(wl.ar[0], non_blocking=True)
-            torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
+        e2e_ms = e2e_leg(torch, rcc, wl, h, Ke)
         barrier(world)
         copy_gbs = copy_bandwidth(torch, device)
     finally:
@@ -365,6 +407,7 @@ def bench_ours(args):
         "rows": rows,
         "e2e": {"value": round(total_e2e / (max_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(max_e2e, 3),
+                "pipeline": "inputs double-buffered; step k+1's H2D copies on 4 streams overlap step k",
                 "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES + 12},
         "gpu_launches": int(launches),
         "clocks": clocks,
@@ -450,6 +493,59 @@ def bench_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def bench_grad_sync_1024(args):
+    """The gradient-sync workload: 4 ranks, 1024 fp32 tensors with sizes
+    log-uniform in [1024, 4194304], grads N(0, 1e-3) x 65536, one AdamW step
+    per iteration (the mean gradient is stored; `--replicas` state copies)."""
+    import torch
+    from gradient_sync_rcc_gb300 import build, rcc, synth
+    build.build()
+    dev = "cuda:0"
+    Rk, P, rep = 4, 1024, args.replicas
+    sizes = synth.param_sizes(P, 1024, 4194304, 20)
+    E = sum(sizes)
+    tensors = []
+    for i, n in enumerate(sizes):
+        g = [synth.gpu_draw("normal:1e-3", n, torch.float32, (22, i, 1, r), dev) * 65536.0
+             for r in range(Rk)]
+        p0 = synth.gpu_draw("normal:0.02", n, torch.float32, (21, i), dev)
+        tensors.append(dict(grads=g, params=[p0.clone() for _ in range(rep)],
+                            exp_avg=[torch.zeros(n, device=dev) for _ in range(rep)],
+                            exp_avg_sq=[torch.zeros(n, device=dev) for _ in range(rep)],
+                            mean_grad=torch.empty(n, device=dev)))
+    sets = rcc.ParamSets(tensors)
+    flags = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH}[args.gs_mode]
+    cfg = rcc.adamw_cfg(replicas=rep, flags=flags)
+    state = rcc.optim_state(scale=65536.0)
+    h = rcc.register(0, Rk, rcc.F32, True)
+    try:
+        for _ in range(max(args.warmup, 3)):
+            rcc.grad_sync_adamw(h, sets, cfg, state)
+        torch.cuda.synchronize()
+        K = args.steps
+        l0 = rcc.launch_count()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        s.record()
+        for _ in range(K):
+            rep_ = rcc.grad_sync_adamw(h, sets, cfg, state)
+        e.record()
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) * 1e3 / K
+        ms = s.elapsed_time(e) / K
+        launches = (rcc.launch_count() - l0) // K
+    finally:
+        rcc.finish(h)
+    traffic = (Rk * 4 + 4) * E + (4 + 24 * rep) * E
+    peak, src = peak_hbm()
+    print(json.dumps({"case": "grad_sync_1024", "mode": args.gs_mode, "ranks": Rk, "tensors": P,
+                      "elements": E, "replicas": rep, "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall, 3),
+                      "launches_per_step": launches, "combine_launches": rep_.combine_launches,
+                      "min_traffic_bytes": traffic,
+                      "traffic_gbs": round(traffic / (ms * 1e-3) / 1e9, 1),
+                      "frac_of_" + src: round(traffic / (ms * 1e-3) / 1e9 / peak, 4)}), flush=True)
+
+
 def bench_case(args):
     """One collective alone, timed with CUDA events; prints one JSON line."""
     import torch
@@ -471,7 +567,7 @@ def bench_case(args):
         outs = [torch.empty(n, dtype=td, device=dev) for _ in range(Rk)]
     traffic = {"all_reduce": 2 * Rk * n * es, "reduce": (Rk + 1) * n * es,
                "broadcast": (Rk + 1) * n * es, "reduce_scatter": (Rk * n + n) * es,
-               "all_gather": (n + Rk * n) * es}.get(c)
+               "all_gather": (n + Rk * n) * es, "all_to_all": 2 * Rk * n * es}.get(c)
     h = rcc.register(0, Rk, dt, not args.fast)
     sets = None
     if c == "grad_sync":
@@ -493,6 +589,8 @@ def bench_case(args):
             rcc.reduce_scatter(h, ins, outs, args.op)
         elif c == "all_gather":
             rcc.all_gather(h, ins, outs)
+        elif c == "all_to_all":
+            rcc.all_to_all_single(h, ins, outs)
         else:
             rcc.grad_sync_adamw(h, sets, cfg, state)
 
@@ -523,6 +621,9 @@ def bench_case(args):
 
 def main():
     args = parse_args()
+    if args.case == "grad_sync_1024":
+        bench_grad_sync_1024(args)
+        return
     if args.case != "step":
         bench_case(args)
         return

@@ -82,6 +82,30 @@ __device__ __forceinline__ void st_vec(void* p, const Vec<W>& v) {
   }
 }
 
+// Schedule knobs (build-time).  RCC_BLOCKED 1 gives each CTA one contiguous
+// range of vectors instead of a grid-stride sweep; RCC_WAVES caps the grid at
+// that many waves of resident CTAs (16 measured best on GB300: with one wave
+// all CTAs drain together and HBM idles at the end; with many, finishing CTAs
+// are replaced at once); RCC_COPY_U overrides the copy pass's vectors per
+// thread; RCC_MIN_BLOCKS (> 0) asks for that many resident CTAs per SM.
+#ifndef RCC_BLOCKED
+#define RCC_BLOCKED 0
+#endif
+#ifndef RCC_WAVES
+#define RCC_WAVES 16
+#endif
+#ifndef RCC_COPY_U
+#define RCC_COPY_U 4
+#endif
+#ifndef RCC_MIN_BLOCKS
+#define RCC_MIN_BLOCKS 0
+#endif
+#if RCC_MIN_BLOCKS > 0
+#define RCC_BOUNDS __launch_bounds__(kThreads, RCC_MIN_BLOCKS)
+#else
+#define RCC_BOUNDS __launch_bounds__(kThreads)
+#endif
+
 // ---- element types ---------------------------------------------------------
 
 // fp32 -> bf16 bits, round to nearest even (hardware cvt); a NaN keeps its
@@ -229,14 +253,21 @@ struct SegView {
   int seg;
   size_t soff, doff;  // element offsets of this segment
   __device__ __forceinline__ const void* src(int q, int eb) const {
+    if (a.a2a_ranks > 0)  // chunk (seg % R) of rank (seg / R)
+      return static_cast<const char*>(a.src[seg / a.a2a_ranks]) +
+             (size_t)(seg % a.a2a_ranks) * a.n * eb;
     const void* base = a.src_per_seg ? a.src[seg] : a.src[q];
     return static_cast<const char*>(base) + soff * eb;
   }
   __device__ __forceinline__ void* dst(int d, int eb) const {
+    if (a.a2a_ranks > 0)  // slot (seg / R) of rank (seg % R)
+      return static_cast<char*>(a.dst[seg % a.a2a_ranks]) + (size_t)(seg / a.a2a_ranks) * a.n * eb;
     void* base = a.dst_per_seg ? a.dst[seg] : a.dst[d];
     return static_cast<char*>(base) + doff * eb;
   }
-  __device__ __forceinline__ int ndst() const { return a.dst_per_seg ? 1 : a.ndst; }
+  __device__ __forceinline__ int ndst() const {
+    return (a.dst_per_seg || a.a2a_ranks > 0) ? 1 : a.ndst;
+  }
 };
 
 // NS > 0: compile-time number of sources (U vectors per thread in flight per
@@ -244,8 +275,7 @@ struct SegView {
 // groups of 8 and folded in rank order.  W: 32-bit words per vector (4 or 8);
 // the host picks 8 only when every address is 32-byte aligned.
 template <typename T, int NS, int RED, bool FAST, int U, int W>
-__global__ void __launch_bounds__(kThreads)
-    mp_kernel(const __grid_constant__ MultiPtrArgs a) {
+__global__ void RCC_BOUNDS mp_kernel(const __grid_constant__ MultiPtrArgs a) {
   using E = Elem<T>;
   constexpr int EPV = W * E::kPerWord;  // elements per vector
   constexpr int VB = 4 * W;             // bytes per vector
@@ -262,13 +292,27 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int q = 0; q < NS; ++q) sp[q] = static_cast<const char*>(sv.src(q, EB));
 
-    for (size_t base = (size_t)blockIdx.x * blockDim.x * U + threadIdx.x; base < nv;
-         base += nthreads * U) {
+    // cyclic: CTAs sweep the range together with a grid-wide stride;
+    // blocked: each CTA walks its own contiguous share
+    const size_t tile = (size_t)blockDim.x * U;
+    size_t first, end, stride;
+    if (RCC_BLOCKED) {
+      const size_t share = (nv + gridDim.x - 1) / gridDim.x;
+      const size_t chunk = (share + tile - 1) / tile * tile;
+      first = (size_t)blockIdx.x * chunk + threadIdx.x;
+      end = (size_t)(blockIdx.x + 1) * chunk < nv ? (size_t)(blockIdx.x + 1) * chunk : nv;
+      stride = tile;
+    } else {
+      first = (size_t)blockIdx.x * tile + threadIdx.x;
+      end = nv;
+      stride = nthreads * U;
+    }
+    for (size_t base = first; base < end; base += stride) {
       Vec<W> v[U][NS];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const size_t idx = base + (size_t)u * blockDim.x;
-        if (idx < nv) {
+        if (idx < end) {
 #pragma unroll
           for (int q = 0; q < NS; ++q) v[u][q] = ld_vec<W>(sp[q] + idx * VB);
         }
@@ -276,7 +320,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const size_t idx = base + (size_t)u * blockDim.x;
-        if (idx < nv) {
+        if (idx < end) {
           Vec<W> out;
           if constexpr (RED == kRedCopy) {
             out = v[u][0];
@@ -362,7 +406,7 @@ __global__ void __launch_bounds__(kThreads)
 // outstanding per thread (U * NS >= 4..8) to cover HBM latency.  32-byte
 // vectors halve U.
 constexpr int unroll_for(int ns, int red) {
-  return red == kRedCopy ? 4 : ns <= 2 ? 4 : ns <= 4 ? 2 : 1;
+  return red == kRedCopy ? RCC_COPY_U : ns <= 2 ? 4 : ns <= 4 ? 2 : 1;
 }
 
 inline int sm_count() {
@@ -413,8 +457,8 @@ cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   const size_t want_tail = (tail + kThreads - 1) / kThreads;
   if (want_tail > want) want = want_tail;
   if (want < 1) want = 1;
-  // one full wave of resident blocks across all segments, sized on the SM count
-  size_t cap = (size_t)resident_blocks((const void*)fn) * sm_count() / (size_t)nseg;
+  // up to RCC_WAVES waves of resident blocks across all segments
+  size_t cap = (size_t)resident_blocks((const void*)fn) * sm_count() * RCC_WAVES / (size_t)nseg;
   if (cap < 1) cap = 1;
   const unsigned gx = (unsigned)(want < cap ? want : cap);
   fn<<<dim3(gx, (unsigned)nseg), kThreads, 0, stream>>>(a);

@@ -248,52 +248,77 @@ template <int REP>  // REP > 0: compile-time replica count; 0: runtime
 __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
   const int rep = REP > 0 ? REP : a.replicas;
   float* const* P = a.state;
+  // With a device decision, the skip flag, the clip coefficient, the step
+  // scalars and the inverse loss scale come from device memory.  They are
+  // fetched first but examined only after this thread's first loads are in
+  // flight, so their latency overlaps the data instead of preceding it.
+  GsDecision d;
+  d.skip = 0u;
+  d.coef = a.clip_coef;
+  AdamWScalars sc = a.s;
+  float inv_scale = a.inv_scale;
+  if (a.decision) {
+    d = *a.decision;
+    sc = *a.dev_scalars;
+    inv_scale = sc.inv_scale;
+  }
+  constexpr int RB = REP > 0 ? REP : 4;  // replicas per batch of loads
   const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
   const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
   const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
   for (uint64_t v = tid; v < nv; v += nthreads) {
-    float gv[4];
+    // the gradient inputs and the first batch of state, all in flight together
+    float4 g4;
     if (a.mean_grad) {
       const uint4 x = ld_vec(a.mean_grad + v * 4);
-      gv[0] = __uint_as_float(x.x);
-      gv[1] = __uint_as_float(x.y);
-      gv[2] = __uint_as_float(x.z);
-      gv[3] = __uint_as_float(x.w);
+      g4 = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                       __uint_as_float(x.w));
     } else {
-      float4 acc = *reinterpret_cast<const float4*>(a.grads[0] + v * 4);
+      g4 = *reinterpret_cast<const float4*>(a.grads[0] + v * 4);
       for (int q = 1; q < a.R; ++q) {
         const float4 y = *reinterpret_cast<const float4*>(a.grads[q] + v * 4);
-        acc.x = __fadd_rn(acc.x, y.x);
-        acc.y = __fadd_rn(acc.y, y.y);
-        acc.z = __fadd_rn(acc.z, y.z);
-        acc.w = __fadd_rn(acc.w, y.w);
+        g4.x = __fadd_rn(g4.x, y.x);
+        g4.y = __fadd_rn(g4.y, y.y);
+        g4.z = __fadd_rn(g4.z, y.z);
+        g4.w = __fadd_rn(g4.w, y.w);
       }
+    }
+    float4 p[RB], m[RB], w[RB];
+#pragma unroll
+    for (int k = 0; k < RB; ++k) {
+      if (k < rep) {
+        p[k] = ld_state(P[k] + v * 4);
+        m[k] = ld_state(P[rep + k] + v * 4);
+        w[k] = ld_state(P[2 * rep + k] + v * 4);
+      }
+    }
+    if (d.skip) return;  // skipped step: state untouched
+    float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+    if (!a.mean_grad) {
       const float Rf = (float)a.R;
-      gv[0] = __fmul_rn(__fdiv_rn(acc.x, Rf), a.inv_scale);
-      gv[1] = __fmul_rn(__fdiv_rn(acc.y, Rf), a.inv_scale);
-      gv[2] = __fmul_rn(__fdiv_rn(acc.z, Rf), a.inv_scale);
-      gv[3] = __fmul_rn(__fdiv_rn(acc.w, Rf), a.inv_scale);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(__fdiv_rn(gv[e], Rf), inv_scale);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], a.clip_coef);
-    constexpr int RB = REP > 0 ? REP : 4;  // replicas per batch of loads
+    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], d.coef);
     for (int r0 = 0; r0 < rep; r0 += RB) {
-      float4 p[RB], m[RB], w[RB];
+      if (r0 > 0) {
 #pragma unroll
-      for (int k = 0; k < RB; ++k) {
-        if (r0 + k < rep) {
-          p[k] = ld_state(P[r0 + k] + v * 4);
-          m[k] = ld_state(P[rep + r0 + k] + v * 4);
-          w[k] = ld_state(P[2 * rep + r0 + k] + v * 4);
+        for (int k = 0; k < RB; ++k) {
+          if (r0 + k < rep) {
+            p[k] = ld_state(P[r0 + k] + v * 4);
+            m[k] = ld_state(P[rep + r0 + k] + v * 4);
+            w[k] = ld_state(P[2 * rep + r0 + k] + v * 4);
+          }
         }
       }
 #pragma unroll
       for (int k = 0; k < RB; ++k) {
         if (r0 + k < rep) {
-          adamw_elem(gv[0], a.s, p[k].x, m[k].x, w[k].x);
-          adamw_elem(gv[1], a.s, p[k].y, m[k].y, w[k].y);
-          adamw_elem(gv[2], a.s, p[k].z, m[k].z, w[k].z);
-          adamw_elem(gv[3], a.s, p[k].w, m[k].w, w[k].w);
+          adamw_elem(gv[0], sc, p[k].x, m[k].x, w[k].x);
+          adamw_elem(gv[1], sc, p[k].y, m[k].y, w[k].y);
+          adamw_elem(gv[2], sc, p[k].z, m[k].z, w[k].z);
+          adamw_elem(gv[3], sc, p[k].w, m[k].w, w[k].w);
           *reinterpret_cast<float4*>(P[r0 + k] + v * 4) = p[k];
           *reinterpret_cast<float4*>(P[rep + r0 + k] + v * 4) = m[k];
           *reinterpret_cast<float4*>(P[2 * rep + r0 + k] + v * 4) = w[k];
@@ -301,6 +326,7 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
       }
     }
   }
+  if (d.skip) return;
   for (uint64_t i = nv * 4 + tid; i < a.numel; i += nthreads) {
     float g;
     if (a.mean_grad) {
@@ -308,12 +334,12 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
     } else {
       float s = a.grads[0][i];
       for (int q = 1; q < a.R; ++q) s = __fadd_rn(s, a.grads[q][i]);
-      g = __fmul_rn(__fdiv_rn(s, (float)a.R), a.inv_scale);
+      g = __fmul_rn(__fdiv_rn(s, (float)a.R), inv_scale);
     }
-    g = __fmul_rn(g, a.clip_coef);
+    g = __fmul_rn(g, d.coef);
     for (int r = 0; r < rep; ++r) {
       float p = P[r][i], m = P[rep + r][i], w = P[2 * rep + r][i];
-      adamw_elem(g, a.s, p, m, w);
+      adamw_elem(g, sc, p, m, w);
       P[r][i] = p;
       P[rep + r][i] = m;
       P[2 * rep + r][i] = w;
@@ -321,11 +347,33 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
   }
 }
 
+// The decision the host would take from the report: skip on any non-finite
+// gradient or norm, otherwise clip when the norm exceeds max_grad_norm.  IEEE
+// double sqrt and division, then one rounding to fp32: the same bits as the
+// host's computation.
+__global__ void gs_decide_kernel(const uint32_t* __restrict__ report, double max_norm,
+                                 GsDecision* __restrict__ out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const double sum_sq = row_sum(report);
+  const double norm = sqrt(sum_sq);
+  const uint32_t skip = (report[2] > 0u || !isfinite(norm)) ? 1u : 0u;
+  float coef = 1.0f;
+  if (!skip && max_norm > 0.0 && norm > max_norm) coef = __double2float_rn(max_norm / norm);
+  out->skip = skip;
+  out->coef = coef;
+}
+
 int sm_count() {
-  int dev = 0, n = 0;
+  static int cached[256] = {};  // per device ordinal; benign race: same value
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  if (dev < 0 || dev >= 256) dev = 0;
+  if (cached[dev] <= 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
 }
 
 }  // namespace gs
@@ -356,11 +404,17 @@ cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* repor
   return cudaGetLastError();
 }
 
+cudaError_t launch_gs_decide(const uint32_t* report, double max_grad_norm, GsDecision* out,
+                             cudaStream_t stream) {
+  gs::gs_decide_kernel<<<1, 32, 0, stream>>>(report, max_grad_norm, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
   const uint64_t units = a.vec_ok ? (a.numel + 3) / 4 : a.numel;
   uint64_t blocks = (units + kThreads - 1) / kThreads;
-  // grid-stride beyond a few full waves of the SMs
-  const uint64_t cap = (uint64_t)gs::sm_count() * 16;
+  // one vector per thread up to 64 CTAs per SM, grid-stride beyond
+  const uint64_t cap = (uint64_t)gs::sm_count() * 64;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   switch (a.replicas) {

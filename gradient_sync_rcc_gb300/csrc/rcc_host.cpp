@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <atomic>
 #include <chrono>
+#include <condition_variable>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -107,6 +108,44 @@ struct Scratch {
   cudaEvent_t report_ev = nullptr;
   cudaEvent_t done_ev = nullptr;    // end of the previous call's work
   bool done_recorded = false;
+  uint64_t desc_gen = 0;            // bumped at every descriptor upload
+  // device decision
+  rcc::GsDecision* decision_dev = nullptr;
+  rcc::AdamWScalars* scalars_dev = nullptr;
+  rcc::AdamWScalars* scalars_host = nullptr;  // pinned staging
+  // captured update launches: a fork/join graph of kBranches parallel chains
+  static constexpr int kBranches = 8;
+  cudaStream_t capture_stream = nullptr;
+  cudaStream_t branch[kBranches] = {};
+  cudaEvent_t fork_ev = nullptr;
+  cudaEvent_t join_ev[kBranches] = {};
+  cudaGraphExec_t graph_exec = nullptr;
+  uint64_t graph_gen = 0;           // desc_gen the graph was captured for
+  size_t graph_P = 0;
+};
+
+// Per-rank arrival: one collective at a time collects each rank's arguments;
+// the last arrival validates and launches, the others wait for its result.
+struct Arrival {
+  int kind;  // 0 all_reduce, 1 reduce, 2 broadcast, 3 reduce_scatter, 4 all_gather
+  const void* send;
+  void* recv;
+  size_t count;
+  int op;
+  int root;
+  cudaStream_t stream;
+};
+
+struct Pending {
+  uint64_t seq = 0;            // number of the collective being collected
+  int arrived = 0;
+  bool launching = false;      // all ranks in; the last one is launching
+  std::vector<char> has;       // per rank: arrived for `seq`
+  std::vector<Arrival> args;
+  // outcome of the most recently completed collective (seq - 1)
+  rcc_status last_status = RCC_OK;
+  std::string last_msg;
+  bool last_launched = false;
 };
 
 struct Session {
@@ -116,7 +155,29 @@ struct Session {
   std::atomic<unsigned> flags;
   std::mutex mu;  // serialises scratch use and teardown
   Scratch sc;
-  Session(int d, int r, rcc_dtype t, unsigned f) : device(d), R(r), dtype(t), flags(f) {}
+  std::mutex pmu;  // guards pend and dead
+  std::condition_variable pcv;
+  Pending pend;
+  bool dead = false;  // finished or reset: waiters give up
+  std::vector<cudaEvent_t> arr_ev;  // one per rank: the rank's stream at arrival
+  cudaEvent_t rank_done_ev = nullptr;  // after the per-rank collective's kernel
+  Session(int d, int r, rcc_dtype t, unsigned f) : device(d), R(r), dtype(t), flags(f) {
+    pend.has.assign(r, 0);
+    pend.args.resize(r);
+  }
+  ~Session() {
+    for (cudaEvent_t e : arr_ev)
+      if (e) cudaEventDestroy(e);
+    if (rank_done_ev) cudaEventDestroy(rank_done_ev);
+  }
+};
+
+// Orders a per-rank collective against every rank's stream: the kernel waits
+// for the work each rank had queued at arrival, and records rank_done_ev.
+struct ArrivalSync {
+  Session* s;
+  const cudaStream_t* streams;  // [R]
+  bool launched = false;
 };
 
 void free_scratch(Scratch& s) {
@@ -128,6 +189,16 @@ void free_scratch(Scratch& s) {
   if (s.desc_host) cudaFreeHost(s.desc_host);
   if (s.report_ev) cudaEventDestroy(s.report_ev);
   if (s.done_ev) cudaEventDestroy(s.done_ev);
+  if (s.decision_dev) cudaFree(s.decision_dev);
+  if (s.scalars_dev) cudaFree(s.scalars_dev);
+  if (s.scalars_host) cudaFreeHost(s.scalars_host);
+  if (s.graph_exec) cudaGraphExecDestroy(s.graph_exec);
+  if (s.capture_stream) cudaStreamDestroy(s.capture_stream);
+  for (int k = 0; k < Scratch::kBranches; ++k) {
+    if (s.branch[k]) cudaStreamDestroy(s.branch[k]);
+    if (s.join_ev[k]) cudaEventDestroy(s.join_ev[k]);
+  }
+  if (s.fork_ev) cudaEventDestroy(s.fork_ev);
   s = Scratch{};
 }
 
@@ -185,6 +256,28 @@ bool overlap(const void* a, size_t an, const void* b, size_t bn) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Byte ranges that must not overlap one another; returns the indices of an
+// overlapping pair, or {-1, -1}.  Sorting keeps this O(n log n) for the R*R
+// outputs of the list all_gather.
+struct Span {
+  uintptr_t lo, hi;
+  int id;
+};
+std::pair<int, int> first_overlap(std::vector<Span> v) {
+  std::sort(v.begin(), v.end(), [](const Span& x, const Span& y) { return x.lo < y.lo; });
+  uintptr_t reach = 0;
+  int reach_id = -1;
+  for (const Span& sp : v) {
+    if (sp.hi == sp.lo) continue;
+    if (reach_id >= 0 && sp.lo < reach) return {reach_id, sp.id};
+    if (sp.hi > reach) {
+      reach = sp.hi;
+      reach_id = sp.id;
+    }
+  }
+  return {-1, -1};
+}
+
 rcc_status check_counts(const size_t* counts, int R, size_t* n) {
   for (int r = 1; r < R; ++r)
     if (counts[r] != counts[0])
@@ -224,13 +317,33 @@ rcc::Red red_of(rcc_op op) {
 }
 
 rcc_status launch(const Session& s, rcc::Red red, int nseg, const MultiPtrArgs& a,
-                  rcc_stream_t stream) {
+                  rcc_stream_t stream, ArrivalSync* sync = nullptr) {
   const bool fast = (s.flags.load() & RCC_DETERMINISTIC) == 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (sync) {
+    Session& ms = *sync->s;
+    if (ms.arr_ev.empty()) ms.arr_ev.assign(ms.R, nullptr);
+    for (int r = 0; r < ms.R; ++r) {
+      cudaError_t e = cudaSuccess;
+      if (!ms.arr_ev[r]) e = cudaEventCreateWithFlags(&ms.arr_ev[r], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventRecord(ms.arr_ev[r], sync->streams[r]);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ms.arr_ev[r], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "arrival ordering");
+    }
+    if (!ms.rank_done_ev) {
+      cudaError_t e = cudaEventCreateWithFlags(&ms.rank_done_ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+    }
+  }
   cudaError_t e = s.dtype == RCC_F32 ? rcc::launch_multi_ptr_f32(red, fast, nseg, a, st)
                                      : rcc::launch_multi_ptr_bf16(red, fast, nseg, a, st);
   if (e != cudaSuccess) return cuda_fail(e, "collective kernel launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (sync) {
+    e = cudaEventRecord(sync->s->rank_done_ev, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    sync->launched = true;
+  }
   return RCC_OK;
 }
 
@@ -247,6 +360,16 @@ int vec_ok(const MultiPtrArgs& a, int nsrc_ptrs, int ndst_ptrs, size_t seg_bytes
 }
 
 }  // namespace
+
+// The session is gone: every rank waiting in a per-rank collective returns
+// RCC_ERR_MISSING_REGISTRATION.
+static void wake_waiters(Session& s) {
+  {
+    std::lock_guard<std::mutex> lock(s.pmu);
+    s.dead = true;
+  }
+  s.pcv.notify_all();
+}
 
 namespace rcc {
 rcc_status set_error(rcc_status st, const char* msg) { return fail(st, "%s", msg); }
@@ -343,6 +466,7 @@ rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream) {
     free_scratch(s->sc);
   }
   unregister(comm);
+  wake_waiters(*s);
   return RCC_OK;
 }
 
@@ -350,6 +474,7 @@ rcc_status rcc_reset(rcc_comm comm) {
   t_err.clear();
   auto s = unregister(comm);
   if (!s) return missing_session();
+  wake_waiters(*s);  // a half-arrived per-rank collective is discarded
   std::lock_guard<std::mutex> lock(s->mu);
   free_scratch(s->sc);
   return RCC_OK;
@@ -357,8 +482,9 @@ rcc_status rcc_reset(rcc_comm comm) {
 
 // ---- collectives ---------------------------------------------------------------
 
-rcc_status rcc_all_reduce(rcc_comm comm, const void* const* send, void* const* recv,
-                          const size_t* counts, const rcc_op* ops, rcc_stream_t stream) {
+static rcc_status all_reduce_impl(rcc_comm comm, const void* const* send, void* const* recv,
+                          const size_t* counts, const rcc_op* ops, rcc_stream_t stream,
+    ArrivalSync* sync) {
   t_err.clear();
   if (!send || !recv || !counts || !ops)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv, counts and ops arrays are required");
@@ -394,12 +520,18 @@ rcc_status rcc_all_reduce(rcc_comm comm, const void* const* send, void* const* r
   a.nsrc = a.ndst = R;
   a.mean_div = ops[0] == RCC_MEAN ? R : 0;
   a.vec_ok = vec_ok(a, R, R, 0, 0);
-  return launch(*s, red_of(ops[0]), 1, a, stream);
+  return launch(*s, red_of(ops[0]), 1, a, stream, sync);
 }
 
-rcc_status rcc_reduce(rcc_comm comm, const void* const* send, void* const* recv,
+rcc_status rcc_all_reduce(rcc_comm comm, const void* const* send, void* const* recv,
+                          const size_t* counts, const rcc_op* ops, rcc_stream_t stream) {
+  return all_reduce_impl(comm, send, recv, counts, ops, stream, nullptr);
+}
+
+static rcc_status reduce_impl(rcc_comm comm, const void* const* send, void* const* recv,
                       const size_t* counts, const rcc_op* ops, const int* roots,
-                      rcc_stream_t stream) {
+                      rcc_stream_t stream,
+    ArrivalSync* sync) {
   t_err.clear();
   if (!send || !recv || !counts || !ops || !roots)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv, counts, ops and roots arrays are required");
@@ -437,11 +569,18 @@ rcc_status rcc_reduce(rcc_comm comm, const void* const* send, void* const* recv,
   a.ndst = 1;
   a.mean_div = ops[0] == RCC_MEAN ? R : 0;
   a.vec_ok = vec_ok(a, R, 1, 0, 0);
-  return launch(*s, red_of(ops[0]), 1, a, stream);
+  return launch(*s, red_of(ops[0]), 1, a, stream, sync);
 }
 
-rcc_status rcc_broadcast(rcc_comm comm, const void* const* send, void* const* recv,
-                         const size_t* counts, rcc_stream_t stream) {
+rcc_status rcc_reduce(rcc_comm comm, const void* const* send, void* const* recv,
+                      const size_t* counts, const rcc_op* ops, const int* roots,
+                      rcc_stream_t stream) {
+  return reduce_impl(comm, send, recv, counts, ops, roots, stream, nullptr);
+}
+
+static rcc_status broadcast_impl(rcc_comm comm, const void* const* send, void* const* recv,
+                         const size_t* counts, rcc_stream_t stream,
+    ArrivalSync* sync) {
   t_err.clear();
   if (!send || !recv || !counts)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and counts arrays are required");
@@ -482,11 +621,17 @@ rcc_status rcc_broadcast(rcc_comm comm, const void* const* send, void* const* re
   a.nsrc = 1;
   a.ndst = nd;
   a.vec_ok = vec_ok(a, 1, nd, 0, 0);
-  return launch(*s, rcc::kRedCopy, 1, a, stream);
+  return launch(*s, rcc::kRedCopy, 1, a, stream, sync);
 }
 
-rcc_status rcc_reduce_scatter(rcc_comm comm, const void* const* send, void* const* recv,
-                              const size_t* in_counts, const rcc_op* ops, rcc_stream_t stream) {
+rcc_status rcc_broadcast(rcc_comm comm, const void* const* send, void* const* recv,
+                         const size_t* counts, rcc_stream_t stream) {
+  return broadcast_impl(comm, send, recv, counts, stream, nullptr);
+}
+
+static rcc_status reduce_scatter_impl(rcc_comm comm, const void* const* send, void* const* recv,
+                              const size_t* in_counts, const rcc_op* ops, rcc_stream_t stream,
+    ArrivalSync* sync) {
   t_err.clear();
   if (!send || !recv || !in_counts || !ops)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv, in_counts and ops arrays are required");
@@ -525,11 +670,17 @@ rcc_status rcc_reduce_scatter(rcc_comm comm, const void* const* send, void* cons
   a.dst_per_seg = 1;
   a.mean_div = ops[0] == RCC_MEAN ? R : 0;
   a.vec_ok = vec_ok(a, R, R, n * es, 0);
-  return launch(*s, red_of(ops[0]), R, a, stream);
+  return launch(*s, red_of(ops[0]), R, a, stream, sync);
 }
 
-rcc_status rcc_all_gather(rcc_comm comm, const void* const* send, void* const* recv,
-                          const size_t* in_counts, rcc_stream_t stream) {
+rcc_status rcc_reduce_scatter(rcc_comm comm, const void* const* send, void* const* recv,
+                              const size_t* in_counts, const rcc_op* ops, rcc_stream_t stream) {
+  return reduce_scatter_impl(comm, send, recv, in_counts, ops, stream, nullptr);
+}
+
+static rcc_status all_gather_impl(rcc_comm comm, const void* const* send, void* const* recv,
+                          const size_t* in_counts, rcc_stream_t stream,
+    ArrivalSync* sync) {
   t_err.clear();
   if (!send || !recv || !in_counts)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and in_counts arrays are required");
@@ -567,7 +718,268 @@ rcc_status rcc_all_gather(rcc_comm comm, const void* const* send, void* const* r
   a.src_per_seg = 1;
   a.dst_seg_stride = n;
   a.vec_ok = vec_ok(a, R, R, 0, n * es);
-  return launch(*s, rcc::kRedCopy, R, a, stream);
+  return launch(*s, rcc::kRedCopy, R, a, stream, sync);
+}
+
+rcc_status rcc_all_gather(rcc_comm comm, const void* const* send, void* const* recv,
+                          const size_t* in_counts, rcc_stream_t stream) {
+  return all_gather_impl(comm, send, recv, in_counts, stream, nullptr);
+}
+
+// ---- all_to_all_single and the list all_gather ---------------------------------
+
+rcc_status rcc_all_to_all_single(rcc_comm comm, const void* const* send, void* const* recv,
+                                 const size_t* in_counts, rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !in_counts)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and in_counts arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t N;
+  rcc_status st = check_counts(in_counts, R, &N);
+  if (st != RCC_OK) return st;
+  if (N % (size_t)R != 0)
+    return fail(RCC_ERR_SHAPE_MISMATCH, "count %zu is not a multiple of %d ranks", N, R);
+  if (N == 0) return RCC_OK;
+  for (int r = 0; r < R; ++r)
+    if (!send[r] || !recv[r])
+      return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no %s buffer", r,
+                  send[r] ? "recv" : "send");
+  const size_t es = elem_bytes(s->dtype), n = N / (size_t)R;
+  std::vector<Span> spans;
+  for (int r = 0; r < R; ++r) {
+    const uintptr_t o = reinterpret_cast<uintptr_t>(recv[r]);
+    spans.push_back({o, o + N * es, r});
+  }
+  auto ov = first_overlap(spans);
+  if (ov.first >= 0)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "recv buffers of ranks %d and %d overlap", ov.first,
+                ov.second);
+  for (int r = 0; r < R; ++r)
+    for (int q = 0; q < R; ++q)
+      if (overlap(recv[r], N * es, send[q], N * es))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "recv of rank %d overlaps send of rank %d", r, q);
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  MultiPtrArgs a{};
+  for (int r = 0; r < R; ++r) {
+    a.src[r] = send[r];
+    a.dst[r] = recv[r];
+  }
+  a.n = n;
+  a.nsrc = 1;
+  a.ndst = 1;
+  a.a2a_ranks = R;
+  a.vec_ok = vec_ok(a, R, R, n * es, 0);
+  return launch(*s, rcc::kRedCopy, R * R, a, stream);
+}
+
+rcc_status rcc_all_gather_list(rcc_comm comm, const void* const* send, void* const* recv,
+                               const size_t* in_counts, rcc_stream_t stream) {
+  t_err.clear();
+  if (!send || !recv || !in_counts)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and in_counts arrays are required");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  const int R = s->R;
+  size_t n;
+  rcc_status st = check_counts(in_counts, R, &n);
+  if (st != RCC_OK) return st;
+  if (n == 0) return RCC_OK;
+  for (int q = 0; q < R; ++q)
+    if (!send[q]) return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no send buffer", q);
+  for (int i = 0; i < R * R; ++i)
+    if (!recv[i])
+      return fail(RCC_ERR_MISSING_REGISTRATION, "rank %d supplies no output for rank %d's tensor",
+                  i / R, i % R);
+  const size_t es = elem_bytes(s->dtype), bytes = n * es;
+  // outputs disjoint from each other and from every input; rank r's own
+  // entry may be its input (in place: nothing to copy)
+  auto in_place = [&](int i) { return i / R == i % R && recv[i] == send[i % R]; };
+  std::vector<Span> spans;
+  for (int i = 0; i < R * R; ++i) {
+    if (in_place(i)) continue;
+    const uintptr_t o = reinterpret_cast<uintptr_t>(recv[i]);
+    spans.push_back({o, o + bytes, i});
+  }
+  auto ov = first_overlap(spans);
+  if (ov.first >= 0)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "outputs %d and %d of the list overlap", ov.first,
+                ov.second);
+  for (int i = 0; i < R * R; ++i)
+    for (int q = 0; q < R && !in_place(i); ++q)
+      if (overlap(recv[i], bytes, send[q], bytes))
+        return fail(RCC_ERR_INVALID_ARGUMENT, "output %d of the list overlaps send of rank %d", i,
+                    q);
+  if ((st = check_device(s->device)) != RCC_OK) return st;
+  // one copy pass per source rank: send[q] -> recv[r*R + q] for every r
+  for (int q = 0; q < R; ++q) {
+    MultiPtrArgs a{};
+    a.src[0] = send[q];
+    int nd = 0;
+    for (int r = 0; r < R; ++r)
+      if (!(r == q && recv[r * R + q] == send[q])) a.dst[nd++] = recv[r * R + q];
+    if (nd == 0) continue;
+    a.n = n;
+    a.nsrc = 1;
+    a.ndst = nd;
+    a.vec_ok = vec_ok(a, 1, nd, 0, 0);
+    if ((st = launch(*s, rcc::kRedCopy, 1, a, stream)) != RCC_OK) return st;
+  }
+  return RCC_OK;
+}
+
+// ---- per-rank arrival ------------------------------------------------------------
+
+}  // extern "C"
+
+namespace {
+
+// Every rank's arguments are in: check they describe one collective and run
+// it through the group implementation, ordered against every rank's stream.
+rcc_status launch_arrived(rcc_comm comm, const Session& s, const std::vector<Arrival>& args,
+                          ArrivalSync* sync, cudaStream_t launch_stream) {
+  const int R = s.R;
+  for (int r = 1; r < R; ++r)
+    if (args[r].kind != args[0].kind)
+      return fail(RCC_ERR_INCONSISTENT_OP, "rank %d called a different collective than rank 0", r);
+  std::vector<const void*> send(R);
+  std::vector<void*> recv(R);
+  std::vector<size_t> counts(R);
+  std::vector<rcc_op> ops(R);
+  std::vector<int> roots(R);
+  std::vector<cudaStream_t> streams(R);
+  for (int r = 0; r < R; ++r) {
+    send[r] = args[r].send;
+    recv[r] = args[r].recv;
+    counts[r] = args[r].count;
+    ops[r] = static_cast<rcc_op>(args[r].op);
+    roots[r] = args[r].root;
+    streams[r] = args[r].stream;
+  }
+  sync->streams = streams.data();
+  rcc_stream_t st = reinterpret_cast<rcc_stream_t>(launch_stream);
+  switch (args[0].kind) {
+    case 0: return all_reduce_impl(comm, send.data(), recv.data(), counts.data(), ops.data(), st, sync);
+    case 1:
+      return reduce_impl(comm, send.data(), recv.data(), counts.data(), ops.data(), roots.data(), st,
+                         sync);
+    case 2: return broadcast_impl(comm, send.data(), recv.data(), counts.data(), st, sync);
+    case 3:
+      return reduce_scatter_impl(comm, send.data(), recv.data(), counts.data(), ops.data(), st, sync);
+    default: return all_gather_impl(comm, send.data(), recv.data(), counts.data(), st, sync);
+  }
+}
+
+void complete(Pending& pd) {
+  ++pd.seq;
+  pd.arrived = 0;
+  pd.launching = false;
+  std::fill(pd.has.begin(), pd.has.end(), 0);
+}
+
+// One rank's arrival: record its arguments; the last rank launches for all,
+// the others wait (bounded) for that outcome and order their stream after it.
+rcc_status rank_arrive(rcc_comm comm, int rank, const Arrival& a) {
+  t_err.clear();
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  if (rank < 0 || rank >= s->R)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "rank %d outside [0, %d)", rank, s->R);
+  std::unique_lock<std::mutex> lk(s->pmu);
+  if (s->dead) return missing_session();
+  Pending& pd = s->pend;
+  if (pd.has[rank])
+    return fail(RCC_ERR_INVALID_ARGUMENT, "rank %d arrived twice for one collective", rank);
+  pd.has[rank] = 1;
+  pd.args[rank] = a;
+  ++pd.arrived;
+  const uint64_t my_seq = pd.seq;
+  if (pd.arrived < s->R) {
+    const auto deadline =
+        std::chrono::steady_clock::now() + std::chrono::milliseconds(wait_limit_ms());
+    while (pd.seq == my_seq && !s->dead) {
+      if (pd.launching) {
+        s->pcv.wait(lk);  // all ranks are in: the outcome is moments away
+        continue;
+      }
+      if (s->pcv.wait_until(lk, deadline) == std::cv_status::timeout && pd.seq == my_seq &&
+          !s->dead && !pd.launching) {
+        // give up: the collective is discarded for every rank waiting on it
+        pd.last_status = RCC_ERR_TIMEOUT;
+        pd.last_msg = "not every rank arrived within the wait limit; collective discarded";
+        pd.last_launched = false;
+        complete(pd);
+        lk.unlock();
+        s->pcv.notify_all();
+        return fail(RCC_ERR_TIMEOUT, "%s", "not every rank arrived within the wait limit; "
+                                           "collective discarded");
+      }
+    }
+    if (pd.seq == my_seq) return missing_session();  // finished or reset meanwhile
+    const rcc_status st = pd.last_status;
+    const std::string msg = pd.last_msg;
+    const bool launched = pd.last_launched;
+    cudaEvent_t done = s->rank_done_ev;
+    lk.unlock();
+    if (st != RCC_OK) {
+      t_err = msg;
+      return st;
+    }
+    if (launched) {
+      cudaError_t e = cudaStreamWaitEvent(a.stream, done, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    return RCC_OK;
+  }
+  pd.launching = true;
+  const std::vector<Arrival> args = pd.args;
+  lk.unlock();
+  ArrivalSync sync{s.get(), nullptr};
+  const rcc_status st = launch_arrived(comm, *s, args, &sync, a.stream);
+  const std::string msg = t_err;
+  lk.lock();
+  pd.last_status = st;
+  pd.last_msg = msg;
+  pd.last_launched = sync.launched;
+  complete(pd);
+  lk.unlock();
+  s->pcv.notify_all();
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+rcc_status rcc_all_reduce_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                               size_t count, rcc_op op, rcc_stream_t stream) {
+  return rank_arrive(comm, rank,
+                     Arrival{0, send, recv, count, (int)op, 0, reinterpret_cast<cudaStream_t>(stream)});
+}
+
+rcc_status rcc_reduce_rank(rcc_comm comm, int rank, const void* send, void* recv, size_t count,
+                           rcc_op op, int root, rcc_stream_t stream) {
+  return rank_arrive(comm, rank, Arrival{1, send, recv, count, (int)op, root,
+                                         reinterpret_cast<cudaStream_t>(stream)});
+}
+
+rcc_status rcc_broadcast_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                              size_t count, rcc_stream_t stream) {
+  return rank_arrive(comm, rank,
+                     Arrival{2, send, recv, count, 0, 0, reinterpret_cast<cudaStream_t>(stream)});
+}
+
+rcc_status rcc_reduce_scatter_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                                   size_t in_count, rcc_op op, rcc_stream_t stream) {
+  return rank_arrive(comm, rank, Arrival{3, send, recv, in_count, (int)op, 0,
+                                         reinterpret_cast<cudaStream_t>(stream)});
+}
+
+rcc_status rcc_all_gather_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                               size_t in_count, rcc_stream_t stream) {
+  return rank_arrive(comm, rank,
+                     Arrival{4, send, recv, in_count, 0, 0, reinterpret_cast<cudaStream_t>(stream)});
 }
 
 // ---- gradient sync + fused AdamW ------------------------------------------------
@@ -613,6 +1025,48 @@ rcc_status ensure_fixed_scratch(Scratch& sc) {
   return RCC_OK;
 }
 
+rcc_status ensure_decision_scratch(Scratch& sc) {
+  cudaError_t e;
+  if (!sc.decision_dev) {
+    e = cudaMalloc(reinterpret_cast<void**>(&sc.decision_dev), sizeof(rcc::GsDecision));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(decision)");
+  }
+  if (!sc.scalars_dev) {
+    e = cudaMalloc(reinterpret_cast<void**>(&sc.scalars_dev), sizeof(rcc::AdamWScalars));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scalars)");
+  }
+  if (!sc.scalars_host) {
+    e = cudaMallocHost(reinterpret_cast<void**>(&sc.scalars_host), sizeof(rcc::AdamWScalars));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(scalars)");
+  }
+  return RCC_OK;
+}
+
+// Host copy of the device decision kernel: the same IEEE double arithmetic.
+void host_decision(double sum_sq, uint32_t nonfinite, double max_grad_norm, double* norm,
+                   bool* skip, float* coef) {
+  *norm = std::sqrt(sum_sq);
+  *skip = nonfinite > 0 || !std::isfinite(*norm);
+  *coef = 1.0f;
+  if (!*skip && max_grad_norm > 0.0 && *norm > max_grad_norm)
+    *coef = (float)(max_grad_norm / *norm);
+}
+
+rcc::AdamWScalars step_scalars(const rcc_adamw_cfg* cfg, int64_t t) {
+  rcc::AdamWScalars s{};
+  const double bc1 = 1.0 - std::pow(cfg->beta1, (double)t);
+  const double bc2 = 1.0 - std::pow(cfg->beta2, (double)t);
+  s.step_size = (float)(cfg->lr / bc1);
+  s.inv_bc2_sqrt = (float)(1.0 / std::sqrt(bc2));
+  s.decay = (float)(1.0 - cfg->lr * cfg->weight_decay);
+  s.beta1 = (float)cfg->beta1;
+  s.one_minus_beta1 = (float)(1.0 - cfg->beta1);
+  s.beta2 = (float)cfg->beta2;
+  s.one_minus_beta2 = (float)(1.0 - cfg->beta2);
+  s.eps = (float)cfg->eps;
+  return s;
+}
+
 bool finite_pos(double x) { return std::isfinite(x) && x > 0.0; }
 
 }  // namespace
@@ -650,7 +1104,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return fail(RCC_ERR_INVALID_ARGUMENT, "gradient sync needs an RCC_F32 session");
   if (rep != 1 && rep != R)
     return fail(RCC_ERR_INVALID_ARGUMENT, "replicas %d must be 1 or %d", rep, R);
-  if (cfg->reserved != 0) return fail(RCC_ERR_INVALID_ARGUMENT, "cfg->reserved must be 0");
+  if (cfg->flags & ~(RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown cfg->flags bits 0x%x", cfg->flags);
   if (!finite_pos(cfg->lr) && cfg->lr != 0.0)
     return fail(RCC_ERR_INVALID_ARGUMENT, "lr must be finite and >= 0");
   if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
@@ -750,6 +1205,18 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     e = cudaMemcpyAsync(sc.desc_dev, sc.desc_host, desc_bytes, cudaMemcpyHostToDevice, cs);
     if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
     sc.last_desc.swap(desc);
+    ++sc.desc_gen;
+  }
+  const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
+  const int64_t t_next = state->step + 1;
+  if (on_device) {
+    // the scalars of step t+1; used only if the device decides not to skip
+    if ((st = ensure_decision_scratch(sc)) != RCC_OK) return st;
+    *sc.scalars_host = step_scalars(cfg, t_next);
+    sc.scalars_host->inv_scale = (float)(1.0 / state->scale);
+    e = cudaMemcpyAsync(sc.scalars_dev, sc.scalars_host, sizeof(rcc::AdamWScalars),
+                        cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "scalar upload");
   }
   const char* dbase = static_cast<const char*>(sc.desc_dev);
   const float inv_scale = (float)(1.0 / state->scale);
@@ -793,19 +1260,117 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       cudaSuccess)
     return cuda_fail(e, "report readback");
   if ((e = cudaEventRecord(sc.report_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+
+  uint64_t device_updates = 0;
+  if (on_device) {
+    // decide on the GPU and enqueue the updates behind it, before waiting
+    if ((e = rcc::launch_gs_decide(sc.report_dev, cfg->max_grad_norm, sc.decision_dev, cs)) !=
+        cudaSuccess)
+      return cuda_fail(e, "decision kernel");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    rcc::GsUpdateArgs ua{};
+    ua.R = R;
+    ua.replicas = rep;
+    ua.inv_scale = inv_scale;
+    ua.clip_coef = 1.0f;
+    ua.decision = sc.decision_dev;
+    ua.dev_scalars = sc.scalars_dev;
+    auto enqueue_one = [&](size_t p, cudaStream_t where) -> cudaError_t {
+      ua.state = reinterpret_cast<float* const*>(dbase + off_state) + p * 3 * rep;
+      ua.mean_grad = params[p].mean_grad;
+      ua.grads = reinterpret_cast<const float* const*>(dbase + off_grads) + p * R;
+      ua.numel = params[p].numel;
+      ua.vec_ok = upd_vec[p];
+      return rcc::launch_gs_update(ua, where);
+    };
+    auto enqueue_updates = [&](cudaStream_t where) -> cudaError_t {
+      for (size_t p = 0; p < P; ++p) {
+        cudaError_t le = enqueue_one(p, where);
+        if (le != cudaSuccess) return le;
+      }
+      return cudaSuccess;
+    };
+    // Inside a capture: fork into parallel chains, largest tensors first onto
+    // the least-loaded chain, then join.  Disjoint tensors, so the update
+    // kernels may run concurrently; small ones no longer wait in a queue.
+    auto enqueue_branched = [&](cudaStream_t origin) -> cudaError_t {
+      cudaError_t le;
+      if (!sc.fork_ev && (le = cudaEventCreateWithFlags(&sc.fork_ev, cudaEventDisableTiming)))
+        return le;
+      for (int k = 0; k < Scratch::kBranches; ++k) {
+        if (!sc.branch[k] &&
+            (le = cudaStreamCreateWithFlags(&sc.branch[k], cudaStreamNonBlocking)) != cudaSuccess)
+          return le;
+        if (!sc.join_ev[k] &&
+            (le = cudaEventCreateWithFlags(&sc.join_ev[k], cudaEventDisableTiming)) != cudaSuccess)
+          return le;
+      }
+      if ((le = cudaEventRecord(sc.fork_ev, origin)) != cudaSuccess) return le;
+      for (int k = 0; k < Scratch::kBranches; ++k)
+        if ((le = cudaStreamWaitEvent(sc.branch[k], sc.fork_ev, 0)) != cudaSuccess) return le;
+      std::vector<size_t> order(P);
+      for (size_t p = 0; p < P; ++p) order[p] = p;
+      std::stable_sort(order.begin(), order.end(),
+                       [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
+      uint64_t load[Scratch::kBranches] = {};
+      for (size_t p : order) {
+        int k = 0;
+        for (int j = 1; j < Scratch::kBranches; ++j)
+          if (load[j] < load[k]) k = j;
+        load[k] += params[p].numel;
+        if ((le = enqueue_one(p, sc.branch[k])) != cudaSuccess) return le;
+      }
+      for (int k = 0; k < Scratch::kBranches; ++k) {
+        if ((le = cudaEventRecord(sc.join_ev[k], sc.branch[k])) != cudaSuccess) return le;
+        if ((le = cudaStreamWaitEvent(origin, sc.join_ev[k], 0)) != cudaSuccess) return le;
+      }
+      return cudaSuccess;
+    };
+    if (cfg->flags & RCC_ADAMW_GRAPH) {
+      if (!sc.graph_exec || sc.graph_gen != sc.desc_gen || sc.graph_P != P) {
+        // capture the P update launches once for these tables
+        if (sc.graph_exec) cudaGraphExecDestroy(sc.graph_exec);
+        sc.graph_exec = nullptr;
+        if (!sc.capture_stream &&
+            (e = cudaStreamCreateWithFlags(&sc.capture_stream, cudaStreamNonBlocking)) != cudaSuccess)
+          return cuda_fail(e, "cudaStreamCreate");
+        if ((e = cudaStreamBeginCapture(sc.capture_stream, cudaStreamCaptureModeThreadLocal)) !=
+            cudaSuccess)
+          return cuda_fail(e, "cudaStreamBeginCapture");
+        cudaError_t le = enqueue_branched(sc.capture_stream);
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamEndCapture(sc.capture_stream, &graph);
+        if (le != cudaSuccess) {
+          if (graph) cudaGraphDestroy(graph);
+          return cuda_fail(le, "update capture");
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+        e = cudaGraphInstantiate(&sc.graph_exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+        sc.graph_gen = sc.desc_gen;
+        sc.graph_P = P;
+      }
+      if ((e = cudaGraphLaunch(sc.graph_exec, cs)) != cudaSuccess)
+        return cuda_fail(e, "cudaGraphLaunch");
+    } else {
+      if ((e = enqueue_updates(cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
+    }
+    device_updates = P;
+    g_launches.fetch_add(P, std::memory_order_relaxed);
+  }
   if ((st = wait_event(sc.report_ev, "12-byte report readback")) != RCC_OK) return st;
 
-  // host decision [RUDA docs, native PyTorch section]: skip on non-finite,
+  // the decision [RUDA docs, native PyTorch section]: skip on non-finite,
   // clip after unscale when the global norm exceeds max_grad_norm
   uint64_t bits = ((uint64_t)sc.report_host[1] << 32) | sc.report_host[0];
   double sum_sq;
   std::memcpy(&sum_sq, &bits, 8);
   const uint32_t nonfinite = sc.report_host[2];
-  const double norm = std::sqrt(sum_sq);
-  const bool skip = nonfinite > 0 || !std::isfinite(norm);
-  float coef = 1.0f;
-  if (!skip && cfg->max_grad_norm > 0.0 && norm > cfg->max_grad_norm)
-    coef = (float)(cfg->max_grad_norm / norm);
+  double norm;
+  bool skip;
+  float coef;
+  host_decision(sum_sq, nonfinite, cfg->max_grad_norm, &norm, &skip, &coef);
 
   rcc_step_report rep_out{};
   rep_out.sum_sq = sum_sq;
@@ -818,22 +1383,21 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   rep_out.stats_rows = total_rows;
   rep_out.combine_region_bytes = region_bytes;
 
+  rep_out.update_launches = device_updates;
   if (skip) {
     state->scale *= state->backoff_factor;
     state->growth_tracker = 0;
+  } else if (on_device) {
+    state->step = t_next;
+    state->growth_tracker += 1;
+    if (state->growth_tracker >= state->growth_interval) {
+      state->scale *= state->growth_factor;
+      state->growth_tracker = 0;
+    }
   } else {
-    const int64_t t = state->step + 1;
-    const double bc1 = 1.0 - std::pow(cfg->beta1, (double)t);
-    const double bc2 = 1.0 - std::pow(cfg->beta2, (double)t);
+    const int64_t t = t_next;
     rcc::GsUpdateArgs ua{};
-    ua.s.step_size = (float)(cfg->lr / bc1);
-    ua.s.inv_bc2_sqrt = (float)(1.0 / std::sqrt(bc2));
-    ua.s.decay = (float)(1.0 - cfg->lr * cfg->weight_decay);
-    ua.s.beta1 = (float)cfg->beta1;
-    ua.s.one_minus_beta1 = (float)(1.0 - cfg->beta1);
-    ua.s.beta2 = (float)cfg->beta2;
-    ua.s.one_minus_beta2 = (float)(1.0 - cfg->beta2);
-    ua.s.eps = (float)cfg->eps;
+    ua.s = step_scalars(cfg, t);
     ua.R = R;
     ua.replicas = rep;
     ua.inv_scale = inv_scale;

@@ -28,6 +28,8 @@ enum Red : int { kRedSum = 0, kRedMax = 1, kRedMin = 2, kRedCopy = 3 };
 //   broadcast       1 segment, 1 source (root), R (or R-1) destinations
 //   reduce_scatter  R segments, R sources at offset s*n, destination recv[s]
 //   all_gather      R segments, source send[s], R destinations at offset s*n
+//   all_to_all      R*R segments (a2a_ranks = R): segment q*R + r copies
+//                   send[q] at offset r*n to recv[r] at offset q*n
 struct MultiPtrArgs {
   const void* src[kMaxRanks];
   void* dst[kMaxRanks];
@@ -38,6 +40,7 @@ struct MultiPtrArgs {
   int ndst;
   int src_per_seg;
   int dst_per_seg;
+  int a2a_ranks; // > 0: all-to-all addressing over this many ranks (see above)
   int mean_div;  // > 0: the sum is divided by this (IEEE division) before storing
   int vec_ok;    // alignment class in bytes (0, 16 or 32): every source and
                  // destination address, with segment offsets, is a multiple of
@@ -86,6 +89,14 @@ struct AdamWScalars {
   float inv_bc2_sqrt;  // 1 / sqrt(1 - beta2^t)
   float decay;         // 1 - lr * wd
   float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+  float inv_scale;     // fl32(1 / S): used by the device-decision flow
+};
+
+// Written on the device by the decision kernel: the step is skipped, or every
+// gradient is multiplied by coef.
+struct GsDecision {
+  uint32_t skip;
+  float coef;
 };
 
 struct GsUpdateArgs {
@@ -100,9 +111,14 @@ struct GsUpdateArgs {
   float inv_scale;
   float clip_coef;
   AdamWScalars s;
+  const GsDecision* decision;       // device decision (skip, coef); NULL: use clip_coef and s
+  const AdamWScalars* dev_scalars;  // device copy of the step scalars, used with decision
 };
 
 cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream);
+// One thread turns the 12-byte report into the decision (same arithmetic as the host).
+cudaError_t launch_gs_decide(const uint32_t* report, double max_grad_norm, GsDecision* out,
+                             cudaStream_t stream);
 
 // Host layer services for entry points defined outside rcc_host.cpp: record
 // the calling thread's error text (returns st), count kernel launches.

@@ -32,13 +32,17 @@ F32, BF16 = 0, 1
 SUM, MEAN, MAX, MIN = 0, 1, 2, 3
 OPS = {"sum": SUM, "mean": MEAN, "max": MAX, "min": MIN}
 DETERMINISTIC = 0x1
+ADAMW_DEVICE_DECISION = 0x1
+ADAMW_GRAPH = 0x2
 MAX_RANKS = 64
 
 # every symbol include/rcc.h declares
 SYMBOLS = ["rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
            "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
            "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc", "rcc_last_error_message",
-           "rcc_status_string", "rcc_kernel_launch_count"]
+           "rcc_status_string", "rcc_kernel_launch_count", "rcc_all_reduce_rank",
+           "rcc_reduce_rank", "rcc_broadcast_rank", "rcc_reduce_scatter_rank",
+           "rcc_all_gather_rank", "rcc_all_to_all_single", "rcc_all_gather_list"]
 
 
 class ParamSet(C.Structure):
@@ -53,7 +57,7 @@ class AdamWCfg(C.Structure):
                 ("eps", C.c_double), ("weight_decay", C.c_double),
                 ("max_grad_norm", C.c_double), ("replicas", C.c_int32),
                 ("hierarchical_stats", C.c_int32), ("elems_per_row", C.c_uint32),
-                ("reserved", C.c_uint32)]
+                ("flags", C.c_uint32)]
 
 
 class OptimState(C.Structure):
@@ -99,9 +103,19 @@ def lib():
                                           C.POINTER(StepReport), C.c_void_p]
         L.rcc_grad_stats_noalloc.argtypes = [_PP, C.c_int, C.c_size_t, C.c_double, C.c_void_p,
                                              C.c_void_p, C.c_void_p]
+        vp, sz = C.c_void_p, C.c_size_t
+        L.rcc_all_reduce_rank.argtypes = [vp, C.c_int, vp, vp, sz, C.c_int, vp]
+        L.rcc_reduce_rank.argtypes = [vp, C.c_int, vp, vp, sz, C.c_int, C.c_int, vp]
+        L.rcc_broadcast_rank.argtypes = [vp, C.c_int, vp, vp, sz, vp]
+        L.rcc_reduce_scatter_rank.argtypes = [vp, C.c_int, vp, vp, sz, C.c_int, vp]
+        L.rcc_all_gather_rank.argtypes = [vp, C.c_int, vp, vp, sz, vp]
+        L.rcc_all_to_all_single.argtypes = [vp, _PP, _PP, C.POINTER(C.c_size_t), vp]
+        L.rcc_all_gather_list.argtypes = [vp, _PP, _PP, C.POINTER(C.c_size_t), vp]
         for name in ("rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
                      "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
-                     "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc"):
+                     "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc", "rcc_all_reduce_rank",
+                     "rcc_reduce_rank", "rcc_broadcast_rank", "rcc_reduce_scatter_rank",
+                     "rcc_all_gather_rank", "rcc_all_to_all_single", "rcc_all_gather_list"):
             getattr(L, name).restype = st
         L.rcc_last_error_message.restype = C.c_char_p
         L.rcc_last_error_message.argtypes = []
@@ -230,12 +244,52 @@ def all_gather(comm, send, recv, stream=None):
                                 size_array([t.numel() for t in send]), _stream(stream)))
 
 
+def all_to_all_single(comm, send, recv, stream=None):
+    _check(lib().rcc_all_to_all_single(comm, ptr_array([_ptr(t) for t in send]),
+                                       ptr_array([_ptr(t) for t in recv]),
+                                       size_array([t.numel() for t in send]), _stream(stream)))
+
+
+def all_gather_list(comm, send, recv_lists, stream=None):
+    """recv_lists[r][q] receives send[q]."""
+    R = len(send)
+    flat = [_ptr(recv_lists[r][q]) for r in range(R) for q in range(R)]
+    _check(lib().rcc_all_gather_list(comm, ptr_array([_ptr(t) for t in send]), ptr_array(flat),
+                                     size_array([t.numel() for t in send]), _stream(stream)))
+
+
+# ------------------------------------------------------------- per-rank arrival (one thread per rank)
+
+def all_reduce_rank(comm, rank, send, recv, op="sum", stream=None):
+    _check(lib().rcc_all_reduce_rank(comm, rank, _ptr(send), _ptr(recv), send.numel(), _op(op),
+                                     _stream(stream)))
+
+
+def reduce_rank(comm, rank, send, recv, root, op="sum", stream=None):
+    _check(lib().rcc_reduce_rank(comm, rank, _ptr(send), _ptr(recv), send.numel(), _op(op), root,
+                                 _stream(stream)))
+
+
+def broadcast_rank(comm, rank, send, recv, count, stream=None):
+    _check(lib().rcc_broadcast_rank(comm, rank, _ptr(send), _ptr(recv), count, _stream(stream)))
+
+
+def reduce_scatter_rank(comm, rank, send, recv, op="sum", stream=None):
+    _check(lib().rcc_reduce_scatter_rank(comm, rank, _ptr(send), _ptr(recv), send.numel(),
+                                         _op(op), _stream(stream)))
+
+
+def all_gather_rank(comm, rank, send, recv, stream=None):
+    _check(lib().rcc_all_gather_rank(comm, rank, _ptr(send), _ptr(recv), send.numel(),
+                                     _stream(stream)))
+
+
 # ------------------------------------------------------------- gradient sync
 
 def adamw_cfg(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=1.0,
-              replicas=1, hierarchical_stats=True, elems_per_row=0):
+              replicas=1, hierarchical_stats=True, elems_per_row=0, flags=0):
     return AdamWCfg(lr, betas[0], betas[1], eps, weight_decay, max_grad_norm, replicas,
-                    1 if hierarchical_stats else 0, elems_per_row, 0)
+                    1 if hierarchical_stats else 0, elems_per_row, flags)
 
 
 def optim_state(scale=65536.0, growth_factor=2.0, backoff_factor=0.5, growth_interval=2000,

@@ -157,6 +157,57 @@ rcc_status rcc_all_gather(rcc_comm comm, const void* const* send,
                           void* const* recv, const size_t* in_counts,
                           rcc_stream_t stream);
 
+/* [Monarch all_to_all_single: split the input, scatter the split list to all
+ * ranks, concatenate what each receives].  Equal splits: in_counts[r] = N
+ * elements per rank, N % R == 0 (else RCC_ERR_SHAPE_MISMATCH), n = N / R;
+ * recv[r] holds N elements and recv[r][q*n + j] = send[q][r*n + j].
+ * No in-place form: outputs must not overlap any input. */
+rcc_status rcc_all_to_all_single(rcc_comm comm, const void* const* send,
+                                 void* const* recv, const size_t* in_counts,
+                                 rcc_stream_t stream);
+
+/* [Monarch all_gather: gather tensors from all ranks into a list of output
+ * tensors].  in_counts[r] = n; recv has R*R entries, row-major by receiving
+ * rank: recv[r*R + q] (n elements) receives send[q].  Rank r's own entry
+ * recv[r*R + r] may be send[r] itself (nothing is copied for it).  One copy
+ * pass per source rank. */
+rcc_status rcc_all_gather_list(rcc_comm comm, const void* const* send,
+                               void* const* recv, const size_t* in_counts,
+                               rcc_stream_t stream);
+
+/* ---- per-rank arrival ------------------------------------------------------
+ * [ruCCL §1, §7 (in_process: logical ranks inside one process), §3: every
+ * rank calls matching collectives in the same order with matching shape, op
+ * and root; Monarch Communicator::new: one thread per rank].
+ * Each logical rank -- typically its own host thread -- calls the *_rank form
+ * with only its own buffers and its own stream.  The call returns once every
+ * rank of the session has arrived: the last arrival checks that all ranks
+ * called the same collective and agree (the group calls' checks and codes;
+ * a different collective on some rank is RCC_ERR_INCONSISTENT_OP), makes the
+ * kernel wait for the work each rank had queued on its stream, launches once,
+ * and every rank's stream then waits for the kernel.  All ranks return the
+ * same status.
+ *   - A rank arriving twice for one collective: RCC_ERR_INVALID_ARGUMENT (to
+ *     that call; the collective keeps waiting for the missing ranks).
+ *   - Not every rank arriving within the wait limit (RCC_WAIT_LIMIT_MS,
+ *     default 120 s): the waiting ranks get RCC_ERR_TIMEOUT and the
+ *     collective is discarded.
+ *   - rcc_reset or rcc_finish while ranks wait: they return
+ *     RCC_ERR_MISSING_REGISTRATION ([ruCCL §4]: reset discards in-flight
+ *     operation state).
+ * Arguments mean what the group call's per-rank entries mean: for reduce only
+ * the root's recv is used; for broadcast exactly one rank passes send. */
+rcc_status rcc_all_reduce_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                               size_t count, rcc_op op, rcc_stream_t stream);
+rcc_status rcc_reduce_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                           size_t count, rcc_op op, int root, rcc_stream_t stream);
+rcc_status rcc_broadcast_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                              size_t count, rcc_stream_t stream);
+rcc_status rcc_reduce_scatter_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                                   size_t in_count, rcc_op op, rcc_stream_t stream);
+rcc_status rcc_all_gather_rank(rcc_comm comm, int rank, const void* send, void* recv,
+                               size_t in_count, rcc_stream_t stream);
+
 /* ---- gradient sync + fused AdamW ----------------------------------------- */
 
 /* One parameter tensor as seen by every rank. */
@@ -181,8 +232,21 @@ typedef struct {
   int32_t hierarchical_stats;  /* 1: fan-in-1024 combines; 0: one flat final reduction */
   uint32_t elems_per_row;      /* elements summarised per statistics row; 0 = 8192;
                                   otherwise a multiple of 4 in [4, 2^24] */
-  uint32_t reserved;           /* must be 0 */
+  uint32_t flags;              /* 0 (the pages' flow) or RCC_ADAMW_* bits below */
 } rcc_adamw_cfg;
+
+/* rcc_adamw_cfg.flags.  By default the call reads the 12-byte report back,
+ * decides on the host, then launches the updates ([RUDA-T]).
+ * RCC_ADAMW_DEVICE_DECISION: one more kernel takes the same decision on the
+ *   GPU from the report (identical arithmetic: IEEE double sqrt and division,
+ *   one rounding to fp32), so the per-tensor updates are enqueued right behind
+ *   the statistics; a skipped step launches updates that return at once.  The
+ *   report is still read back before the call returns.
+ * RCC_ADAMW_GRAPH: as DEVICE_DECISION, and the per-tensor update launches are
+ *   captured once into a CUDA graph and replayed while the tensors' pointers
+ *   and sizes stay the same (still one kernel node per parameter tensor). */
+#define RCC_ADAMW_DEVICE_DECISION 0x1u
+#define RCC_ADAMW_GRAPH 0x2u
 
 /* Optimizer step count and GradScaler state, owned by the caller, updated by
  * each call ([RUDA-T]: scale -> step -> update on the same GradScaler). */

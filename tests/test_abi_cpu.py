@@ -308,6 +308,8 @@ def test_grad_sync_validation(L, comm):
     assert gs(arr, cfg=L.adamw_cfg(replicas=R, elems_per_row=6)) == L.ERR_INVALID_ARGUMENT
     assert gs(arr, cfg=L.adamw_cfg(replicas=R, eps=0.0)) == L.ERR_INVALID_ARGUMENT
     assert gs(arr, cfg=L.adamw_cfg(replicas=R, betas=(1.0, 0.999))) == L.ERR_INVALID_ARGUMENT
+    assert gs(arr, cfg=L.adamw_cfg(replicas=R, flags=0x4)) == L.ERR_INVALID_ARGUMENT
+    assert reached_device_check(L, gs(arr, cfg=L.adamw_cfg(replicas=R, flags=L.ADAMW_GRAPH)))
     assert gs(arr, state=L.optim_state(scale=0.0)) == L.ERR_INVALID_ARGUMENT
     assert gs(arr, state=L.optim_state(scale=float("inf"))) == L.ERR_INVALID_ARGUMENT
     # more statistics rows than two fan-in-1024 levels can take
@@ -339,3 +341,52 @@ def test_no_kernel_launched_by_validation(L, comm):
         L.raw("rcc_reduce_scatter", h, S, Rv, n, L.int_array([op] * R), None)
     L.raw("rcc_all_gather", h, S, Rv, n, None)
     assert L.launch_count() == before
+
+
+# ---------------------------------------------------------------- all_to_all / list all_gather
+
+def test_all_to_all_single_errors(L, comm):
+    R = 4
+    h = comm(R)
+    S, Rv = L.ptr_array(addrs(R)), L.ptr_array(addrs(R, base=BASE * 2))
+
+    def a2a(counts, recv=Rv, send=S):
+        return L.raw("rcc_all_to_all_single", h, send, recv, L.size_array(counts), None)
+
+    assert a2a([1002] * R) == L.ERR_SHAPE_MISMATCH
+    assert a2a([1000, 1000, 1000, 996]) == L.ERR_SHAPE_MISMATCH
+    assert a2a([0] * R, recv=L.ptr_array([None] * R)) == L.OK
+    assert a2a([1000] * R, recv=L.ptr_array([None] + addrs(R, base=BASE * 2)[1:])) == \
+        L.ERR_MISSING_REGISTRATION
+    ov = addrs(R, base=BASE * 2)
+    ov[3] = ov[2] + 64
+    assert a2a([1000] * R, recv=L.ptr_array(ov)) == L.ERR_INVALID_ARGUMENT
+    assert a2a([1000] * R, recv=S) == L.ERR_INVALID_ARGUMENT        # no in-place form
+    assert reached_device_check(L, a2a([1000] * R))
+
+
+def test_all_gather_list_errors(L, comm):
+    R = 3
+    h = comm(R)
+    n = 100
+    send = addrs(R)
+    recv = [BASE * 2 + i * 4096 for i in range(R * R)]
+
+    def agl(recv=recv, send=send):
+        return L.raw("rcc_all_gather_list", h, L.ptr_array(send), L.ptr_array(recv),
+                     L.size_array([n] * R), None)
+
+    assert reached_device_check(L, agl())
+    inplace = list(recv)
+    for r in range(R):
+        inplace[r * R + r] = send[r]                    # own entry is the input
+    assert reached_device_check(L, agl(inplace))
+    bad = list(recv)
+    bad[5] = recv[4] + 8                                # two list entries overlap
+    assert agl(bad) == L.ERR_INVALID_ARGUMENT
+    bad = list(recv)
+    bad[1] = send[1]                                    # rank 0's entry aliases rank 1's input
+    assert agl(bad) == L.ERR_INVALID_ARGUMENT
+    bad = list(recv)
+    bad[7] = None
+    assert agl(bad) == L.ERR_MISSING_REGISTRATION

@@ -396,3 +396,56 @@ def test_finish_then_reregister_and_reset_with_pending_work():
     rcc.all_reduce(h2, ins, outs, "sum")
     rcc.finish(h2)
     assert bool(torch.all(outs[0] == 8.0))
+
+
+# ---------------------------------------------------------------- all_to_all_single, list all_gather
+
+@pytest.mark.parametrize("R,n", [(1, 100), (2, 4099), (3, 257), (4, 1 << 16), (8, 33), (8, 1 << 18)])
+@pytest.mark.parametrize("dtype", [rcc.F32, rcc.BF16])
+def test_all_to_all_single(orc, R, n, dtype):
+    td = tdtype(dtype)
+    N = R * n
+    kind = "uniform" if dtype == rcc.F32 else "bf16_uniform"
+    xs = host_ranks(kind, R, N, 1400, R, n)
+    ins = [to_dev(x) for x in xs]
+    outs = [Guarded(N, td) for _ in range(R)]
+    with session(R, dtype, True) as h:
+        rcc.all_to_all_single(h, ins, [o.t for o in outs])
+        torch.cuda.synchronize()
+    want = orc.all_to_all(xs)
+    for r in range(R):
+        assert outs[r].guards_intact()
+        assert bits_equal(to_host(outs[r].t), want[r])
+
+
+def test_all_to_all_single_misaligned(orc):
+    R, n = 4, 1001
+    xs = host_ranks("uniform", R, R * n, 1401)
+    ins = [Guarded(R * n, torch.float32, offset_elems=1, fill=to_dev(x)) for x in xs]
+    outs = [Guarded(R * n, torch.float32, offset_elems=3) for _ in range(R)]
+    with session(R) as h:
+        rcc.all_to_all_single(h, [g.t for g in ins], [o.t for o in outs])
+        torch.cuda.synchronize()
+    want = orc.all_to_all(xs)
+    for r in range(R):
+        assert outs[r].guards_intact() and bits_equal(to_host(outs[r].t), want[r])
+
+
+@pytest.mark.parametrize("R,n", [(2, 1000), (4, 4097), (8, 1 << 16)])
+def test_all_gather_list(orc, R, n):
+    xs = host_ranks("uniform", R, n, 1402, R)
+    ins = [to_dev(x) for x in xs]
+    lists = [[Guarded(n, torch.float32) for _ in range(R)] for _ in range(R)]
+    # rank 1 gathers its own tensor in place
+    lists[1][1] = None
+    recv = [[g.t if g is not None else None for g in row] for row in lists]
+    recv[1][1] = ins[1]
+    with session(R) as h:
+        rcc.all_gather_list(h, ins, recv)
+        torch.cuda.synchronize()
+    for r in range(R):
+        for q in range(R):
+            got = to_host(recv[r][q])
+            assert bits_equal(got, xs[q]), (r, q)
+            if lists[r][q] is not None:
+                assert lists[r][q].guards_intact()

@@ -100,8 +100,8 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
                 assert abs(rep.sum_sq - want) <= 1e-12 * want, (rep.sum_sq, want)
                 assert abs(rep.clip_coef - d.clip_coef) <= 2e-7 * d.clip_coef
                 assert rep.update_launches == len(prob.sizes)
-            else:
-                assert rep.update_launches == 0
+            else:   # the host flow launches nothing; the device flow's updates return at once
+                assert rep.update_launches == (0 if cfg.flags == 0 else len(prob.sizes))
             if check_each or k == steps:
                 for i in range(len(prob.sizes)):
                     t = prob.tensors[i]
@@ -115,18 +115,56 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
     return reports, state
 
 
+MODES = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("replicas", [1, 4])
 @pytest.mark.parametrize("mean_grad", [True, False])
-def test_ten_steps_nan_at_seven(orc, replicas, mean_grad):
+def test_ten_steps_nan_at_seven(orc, replicas, mean_grad, mode):
     sizes = synth.param_sizes(16, 1024, 65536, 10)
     prob = Problem(4, sizes, 11, replicas, mean_grad)
     # the unscaled mean gradient has norm ~0.2 here: max_grad_norm 0.1 keeps
     # the clip active on every applied step
-    reports, state = run_steps(orc, prob, 10, 7, {}, max_norm=0.1)
+    reports, state = run_steps(orc, prob, 10, 7, {"flags": MODES[mode]}, max_norm=0.1)
     assert [r.skipped for r in reports] == [0] * 6 + [1] + [0] * 3
     assert state.step == 9 and state.scale == 32768.0
     assert all(r.combine_launches == 0 for r in reports)      # <= 1024 rows
     assert all(r.clip_coef < 1.0 for r in reports if not r.skipped)
+
+
+def test_decision_modes_bitwise_identical():
+    """Host decision, device decision and the captured graph give the same bits."""
+    sizes = synth.param_sizes(64, 1024, 200000, 30)
+    finals = {}
+    for mode, flags in MODES.items():
+        prob = Problem(4, sizes, 31, 4, mode != "device")
+        cfg = rcc.adamw_cfg(replicas=4, flags=flags)
+        state = rcc.optim_state(scale=65536.0)
+        with session(4) as h:
+            for k in range(1, 7):
+                prob.load_grads(prob.host_grads(k, state.scale, nan_at=4))
+                rep = rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+                assert rep.skipped == (1 if k == 4 else 0)
+            torch.cuda.synchronize()
+        assert state.step == 5
+        finals[mode] = [torch.cat([t["params"][1], t["exp_avg"][0], t["exp_avg_sq"][1]]).cpu()
+                        for t in prob.tensors]
+    for mode in ("device", "graph"):
+        for a, b in zip(finals["host"], finals[mode]):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), mode
+
+
+def test_graph_recaptured_when_tensors_change(orc):
+    """New gradient buffers change the descriptor tables; the graph must follow."""
+    sizes = [10000, 2000, 777]
+    prob = Problem(2, sizes, 32, 1, True)
+    run_steps(orc, prob, 2, None, {"flags": rcc.ADAMW_GRAPH})
+    for t in prob.tensors:
+        t["grads"] = [torch.empty_like(g) for g in t["grads"]]
+        t["mean_grad"] = torch.empty_like(t["mean_grad"])
+    prob.sets = rcc.ParamSets(prob.tensors)
+    run_steps(orc, prob, 2, None, {"flags": rcc.ADAMW_GRAPH})
 
 
 def test_mean_grad_output_bitwise(orc):
