@@ -74,6 +74,9 @@ def parse_args():
     ap.add_argument("--op", default="sum", choices=["sum", "mean", "max", "min"])
     ap.add_argument("--fast", action="store_true", help="pairwise-tree sums instead of rank order")
     ap.add_argument("--replicas", type=int, default=1, help="optimizer-state copies (grad_sync_1024)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="size sweep: all_reduce mean (fp32, bf16), broadcast root 0 and reduce "
+                         "root R-1 for R in {2,4,8}, N = 257*4^k and 2^28; one JSON line per point")
     ap.add_argument("--gs-mode", default="host", choices=["host", "device", "graph"],
                     help="grad-sync decision: host readback (default), device kernel, or device "
                          "kernel + captured update launches")
@@ -619,8 +622,63 @@ def bench_case(args):
                       "min_traffic_bytes": traffic}), flush=True)
 
 
+def bench_sweep(args):
+    """The size sweep of the collectives (one process, CUDA-event timing, median)."""
+    import torch
+    from gradient_sync_rcc_gb300 import build, rcc, synth
+    build.build()
+    dev = "cuda:0"
+    peak, src = peak_hbm()
+    sizes = [257 * 4 ** k for k in range(10)] + [1 << 28]
+    for Rk in (2, 4, 8):
+        for n in sizes:
+            for case, dt in (("all_reduce_mean", rcc.F32), ("all_reduce_mean", rcc.BF16),
+                             ("broadcast", rcc.F32), ("reduce", rcc.F32)):
+                td = torch.float32 if dt == rcc.F32 else torch.bfloat16
+                es = 4 if dt == rcc.F32 else 2
+                ins = synth.gpu_rank_buffers("uniform", Rk, n, td, (5, Rk, n), dev)
+                outs = [torch.empty(n, dtype=td, device=dev) for _ in range(Rk)]
+                h = rcc.register(0, Rk, dt, True)
+                try:
+                    if case == "all_reduce_mean":
+                        fn = lambda: rcc.all_reduce(h, ins, outs, "mean")
+                        traffic = 2 * Rk * n * es
+                    elif case == "broadcast":
+                        fn = lambda: rcc.broadcast(h, ins[0], outs, root=0)
+                        traffic = (Rk + 1) * n * es
+                    else:
+                        fn = lambda: rcc.reduce(h, ins, outs[Rk - 1], root=Rk - 1, op="mean")
+                        traffic = (Rk + 1) * n * es
+                    reps = 50 if traffic < (1 << 30) else 10
+                    for _ in range(3):
+                        fn()
+                    torch.cuda.synchronize()
+                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+                    ev[0].record()
+                    for k in range(reps):
+                        fn()
+                        ev[k + 1].record()
+                    torch.cuda.synchronize()
+                    ms = statistics.median(ev[k].elapsed_time(ev[k + 1]) for k in range(reps))
+                finally:
+                    rcc.finish(h)
+                gbs = traffic / (ms * 1e-3) / 1e9
+                print(json.dumps({"sweep": case, "ranks": Rk, "elems": n,
+                                  "dtype": "f32" if dt == rcc.F32 else "bf16",
+                                  "median_ms": round(ms, 5),
+                                  "algbw_gbs": round(Rk * n * es / (ms * 1e-3) / 1e9, 1),
+                                  "traffic_gbs": round(gbs, 1),
+                                  "frac_of_" + src: round(gbs / peak, 4),
+                                  "l2_resident": traffic < 129e6}), flush=True)
+                del ins, outs
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        bench_sweep(args)
+        return
     if args.case == "grad_sync_1024":
         bench_grad_sync_1024(args)
         return

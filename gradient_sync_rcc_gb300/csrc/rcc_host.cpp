@@ -278,6 +278,25 @@ std::pair<int, int> first_overlap(std::vector<Span> v) {
   return {-1, -1};
 }
 
+// Byte ranges, each written or only read; returns true if a written range
+// overlaps any other range (read-only ranges may overlap each other).
+struct RwSpan {
+  uintptr_t lo, hi;
+  bool written;
+};
+bool written_overlap(std::vector<RwSpan> v) {
+  std::sort(v.begin(), v.end(), [](const RwSpan& x, const RwSpan& y) { return x.lo < y.lo; });
+  uintptr_t reach_w = 0, reach_any = 0;
+  for (const RwSpan& sp : v) {
+    if (sp.hi == sp.lo) continue;
+    if (sp.lo < reach_w) return true;                 // inside an earlier written range
+    if (sp.written && sp.lo < reach_any) return true;  // a written range inside any earlier one
+    if (sp.written && sp.hi > reach_w) reach_w = sp.hi;
+    if (sp.hi > reach_any) reach_any = sp.hi;
+  }
+  return false;
+}
+
 rcc_status check_counts(const size_t* counts, int R, size_t* n) {
   for (int r = 1; r < R; ++r)
     if (counts[r] != counts[0])
@@ -1200,6 +1219,30 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     e = cudaStreamWaitEvent(cs, sc.done_ev, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
+  if (sc.last_desc != desc) {
+    // new tensors: the state and mean-gradient buffers (written) may not
+    // overlap each other or any gradient (gradients are only read)
+    std::vector<RwSpan> spans;
+    spans.reserve(P * (R + 3 * rep + 1));
+    for (size_t p = 0; p < P; ++p) {
+      const rcc_param_set& ps = params[p];
+      const size_t bytes = ps.numel * sizeof(float);
+      auto add = [&](const void* ptr, bool w) {
+        const uintptr_t o = reinterpret_cast<uintptr_t>(ptr);
+        spans.push_back({o, o + bytes, w});
+      };
+      for (int r = 0; r < R; ++r) add(ps.grads[r], false);
+      for (int k = 0; k < rep; ++k) {
+        add(ps.params[k], true);
+        add(ps.exp_avg[k], true);
+        add(ps.exp_avg_sq[k], true);
+      }
+      if (ps.mean_grad) add(ps.mean_grad, true);
+    }
+    if (written_overlap(std::move(spans)))
+      return fail(RCC_ERR_INVALID_ARGUMENT,
+                  "a parameter, moment or mean-gradient buffer overlaps another buffer");
+  }
   if (dev_grew || sc.last_desc != desc) {
     std::memcpy(sc.desc_host, desc.data(), desc_bytes);
     e = cudaMemcpyAsync(sc.desc_dev, sc.desc_host, desc_bytes, cudaMemcpyHostToDevice, cs);
@@ -1261,6 +1304,57 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return cuda_fail(e, "report readback");
   if ((e = cudaEventRecord(sc.report_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
 
+  // One update kernel per tensor, spread over parallel chains forked from
+  // (and joined back into) `origin`: largest tensors first onto the least
+  // loaded chain.  The tensors are disjoint (checked above), so their kernels
+  // may run concurrently and the many small ones no longer queue one behind
+  // another.
+  rcc::GsUpdateArgs ua{};
+  ua.R = R;
+  ua.replicas = rep;
+  ua.inv_scale = inv_scale;
+  auto enqueue_one = [&](size_t p, cudaStream_t where) -> cudaError_t {
+    ua.state = reinterpret_cast<float* const*>(dbase + off_state) + p * 3 * rep;
+    ua.mean_grad = params[p].mean_grad;
+    ua.grads = reinterpret_cast<const float* const*>(dbase + off_grads) + p * R;
+    ua.numel = params[p].numel;
+    ua.vec_ok = upd_vec[p];
+    return rcc::launch_gs_update(ua, where);
+  };
+  auto enqueue_branched = [&](cudaStream_t origin) -> cudaError_t {
+    cudaError_t le;
+    if (!sc.fork_ev && (le = cudaEventCreateWithFlags(&sc.fork_ev, cudaEventDisableTiming)))
+      return le;
+    for (int k = 0; k < Scratch::kBranches; ++k) {
+      if (!sc.branch[k] &&
+          (le = cudaStreamCreateWithFlags(&sc.branch[k], cudaStreamNonBlocking)) != cudaSuccess)
+        return le;
+      if (!sc.join_ev[k] &&
+          (le = cudaEventCreateWithFlags(&sc.join_ev[k], cudaEventDisableTiming)) != cudaSuccess)
+        return le;
+    }
+    if ((le = cudaEventRecord(sc.fork_ev, origin)) != cudaSuccess) return le;
+    for (int k = 0; k < Scratch::kBranches; ++k)
+      if ((le = cudaStreamWaitEvent(sc.branch[k], sc.fork_ev, 0)) != cudaSuccess) return le;
+    std::vector<size_t> order(P);
+    for (size_t p = 0; p < P; ++p) order[p] = p;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
+    uint64_t load[Scratch::kBranches] = {};
+    for (size_t p : order) {
+      int k = 0;
+      for (int j = 1; j < Scratch::kBranches; ++j)
+        if (load[j] < load[k]) k = j;
+      load[k] += params[p].numel;
+      if ((le = enqueue_one(p, sc.branch[k])) != cudaSuccess) return le;
+    }
+    for (int k = 0; k < Scratch::kBranches; ++k) {
+      if ((le = cudaEventRecord(sc.join_ev[k], sc.branch[k])) != cudaSuccess) return le;
+      if ((le = cudaStreamWaitEvent(origin, sc.join_ev[k], 0)) != cudaSuccess) return le;
+    }
+    return cudaSuccess;
+  };
+
   uint64_t device_updates = 0;
   if (on_device) {
     // decide on the GPU and enqueue the updates behind it, before waiting
@@ -1268,64 +1362,9 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
         cudaSuccess)
       return cuda_fail(e, "decision kernel");
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    rcc::GsUpdateArgs ua{};
-    ua.R = R;
-    ua.replicas = rep;
-    ua.inv_scale = inv_scale;
     ua.clip_coef = 1.0f;
     ua.decision = sc.decision_dev;
     ua.dev_scalars = sc.scalars_dev;
-    auto enqueue_one = [&](size_t p, cudaStream_t where) -> cudaError_t {
-      ua.state = reinterpret_cast<float* const*>(dbase + off_state) + p * 3 * rep;
-      ua.mean_grad = params[p].mean_grad;
-      ua.grads = reinterpret_cast<const float* const*>(dbase + off_grads) + p * R;
-      ua.numel = params[p].numel;
-      ua.vec_ok = upd_vec[p];
-      return rcc::launch_gs_update(ua, where);
-    };
-    auto enqueue_updates = [&](cudaStream_t where) -> cudaError_t {
-      for (size_t p = 0; p < P; ++p) {
-        cudaError_t le = enqueue_one(p, where);
-        if (le != cudaSuccess) return le;
-      }
-      return cudaSuccess;
-    };
-    // Inside a capture: fork into parallel chains, largest tensors first onto
-    // the least-loaded chain, then join.  Disjoint tensors, so the update
-    // kernels may run concurrently; small ones no longer wait in a queue.
-    auto enqueue_branched = [&](cudaStream_t origin) -> cudaError_t {
-      cudaError_t le;
-      if (!sc.fork_ev && (le = cudaEventCreateWithFlags(&sc.fork_ev, cudaEventDisableTiming)))
-        return le;
-      for (int k = 0; k < Scratch::kBranches; ++k) {
-        if (!sc.branch[k] &&
-            (le = cudaStreamCreateWithFlags(&sc.branch[k], cudaStreamNonBlocking)) != cudaSuccess)
-          return le;
-        if (!sc.join_ev[k] &&
-            (le = cudaEventCreateWithFlags(&sc.join_ev[k], cudaEventDisableTiming)) != cudaSuccess)
-          return le;
-      }
-      if ((le = cudaEventRecord(sc.fork_ev, origin)) != cudaSuccess) return le;
-      for (int k = 0; k < Scratch::kBranches; ++k)
-        if ((le = cudaStreamWaitEvent(sc.branch[k], sc.fork_ev, 0)) != cudaSuccess) return le;
-      std::vector<size_t> order(P);
-      for (size_t p = 0; p < P; ++p) order[p] = p;
-      std::stable_sort(order.begin(), order.end(),
-                       [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
-      uint64_t load[Scratch::kBranches] = {};
-      for (size_t p : order) {
-        int k = 0;
-        for (int j = 1; j < Scratch::kBranches; ++j)
-          if (load[j] < load[k]) k = j;
-        load[k] += params[p].numel;
-        if ((le = enqueue_one(p, sc.branch[k])) != cudaSuccess) return le;
-      }
-      for (int k = 0; k < Scratch::kBranches; ++k) {
-        if ((le = cudaEventRecord(sc.join_ev[k], sc.branch[k])) != cudaSuccess) return le;
-        if ((le = cudaStreamWaitEvent(origin, sc.join_ev[k], 0)) != cudaSuccess) return le;
-      }
-      return cudaSuccess;
-    };
     if (cfg->flags & RCC_ADAMW_GRAPH) {
       if (!sc.graph_exec || sc.graph_gen != sc.desc_gen || sc.graph_P != P) {
         // capture the P update launches once for these tables
@@ -1354,7 +1393,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       if ((e = cudaGraphLaunch(sc.graph_exec, cs)) != cudaSuccess)
         return cuda_fail(e, "cudaGraphLaunch");
     } else {
-      if ((e = enqueue_updates(cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
+      if ((e = enqueue_branched(cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
     }
     device_updates = P;
     g_launches.fetch_add(P, std::memory_order_relaxed);
@@ -1396,22 +1435,10 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     }
   } else {
     const int64_t t = t_next;
-    rcc::GsUpdateArgs ua{};
     ua.s = step_scalars(cfg, t);
-    ua.R = R;
-    ua.replicas = rep;
-    ua.inv_scale = inv_scale;
     ua.clip_coef = coef;
-    // one update kernel per parameter tensor
-    for (size_t p = 0; p < P; ++p) {
-      ua.state = reinterpret_cast<float* const*>(dbase + off_state) + p * 3 * rep;
-      ua.mean_grad = params[p].mean_grad;
-      ua.grads = reinterpret_cast<const float* const*>(dbase + off_grads) + p * R;
-      ua.numel = params[p].numel;
-      ua.vec_ok = upd_vec[p];
-      if ((e = rcc::launch_gs_update(ua, cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
+    if ((e = enqueue_branched(cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
+    g_launches.fetch_add(P, std::memory_order_relaxed);
     rep_out.update_launches = P;
     state->step = t;
     state->growth_tracker += 1;

@@ -313,3 +313,29 @@ def test_full_1024_tensors_ten_steps(orc):
             assert torch.equal(p_dev[i][j], p_dev[i][0])
     assert bad == 0
     assert math.isfinite(rep.grad_norm)
+
+
+def test_overlapping_outputs_rejected_shared_grads_allowed():
+    """Updates of different tensors may run concurrently, so written buffers
+    (params, moments, mean gradient) must be disjoint from every other buffer;
+    gradients are only read and may be shared."""
+    R, n = 2, 1000
+    g = torch.randn(n, device=DEV)
+    base = torch.zeros(5 * n, device=DEV)
+    t1 = dict(grads=[g, g], params=[base[:n]], exp_avg=[base[n:2 * n]],
+              exp_avg_sq=[base[2 * n:3 * n]], mean_grad=None)
+    clash = dict(grads=[g, g], params=[base[2 * n + 8:3 * n + 8]],
+                 exp_avg=[torch.zeros(n, device=DEV)], exp_avg_sq=[torch.zeros(n, device=DEV)],
+                 mean_grad=None)
+    fine = dict(grads=[g, g], params=[base[3 * n:4 * n]], exp_avg=[torch.zeros(n, device=DEV)],
+                exp_avg_sq=[torch.zeros(n, device=DEV)], mean_grad=None)
+    mean_on_grad = dict(fine, mean_grad=g)
+    cfg = rcc.adamw_cfg(replicas=1)
+    with session(R) as h:
+        for bad in (clash, mean_on_grad):
+            with pytest.raises(rcc.RccError) as ei:
+                rcc.grad_sync_adamw(h, rcc.ParamSets([t1, bad]), cfg, rcc.optim_state(scale=1.0))
+            assert ei.value.status == rcc.ERR_INVALID_ARGUMENT
+        rep = rcc.grad_sync_adamw(h, rcc.ParamSets([t1, fine]), cfg, rcc.optim_state(scale=1.0))
+        torch.cuda.synchronize()
+    assert rep.update_launches == 2
