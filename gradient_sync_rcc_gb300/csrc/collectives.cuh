@@ -129,6 +129,8 @@ template <>
 struct Elem<float> {
   static constexpr int kBytes = 4;
   static constexpr int kPerWord = 1;
+  __device__ static __forceinline__ float lane(uint32_t w, int) { return __uint_as_float(w); }
+  __device__ static __forceinline__ uint32_t pack_word(const float* f) { return __float_as_uint(f[0]); }
   template <int W>
   __device__ static __forceinline__ void unpack(const Vec<W>& v, float* f) {
 #pragma unroll
@@ -156,6 +158,11 @@ template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kBytes = 2;
   static constexpr int kPerWord = 2;
+  // lane 0 is the low half of the word, lane 1 the high half
+  __device__ static __forceinline__ float lane(uint32_t w, int l) {
+    return __uint_as_float(l == 0 ? (w << 16) : (w & 0xFFFF0000u));
+  }
+  __device__ static __forceinline__ uint32_t pack_word(const float* f) { return bf16x2_rn(f[0], f[1]); }
   template <int W>
   __device__ static __forceinline__ void unpack(const Vec<W>& v, float* f) {
 #pragma unroll
@@ -325,18 +332,20 @@ __global__ void RCC_BOUNDS mp_kernel(const __grid_constant__ MultiPtrArgs a) {
           if constexpr (RED == kRedCopy) {
             out = v[u][0];
           } else {
-            float f[NS][EPV];
+            // word by word: unpack one 32-bit word of every rank, reduce its
+            // lanes, pack; only one word's lanes are live at a time
 #pragma unroll
-            for (int q = 0; q < NS; ++q) E::template unpack<W>(v[u][q], f[q]);
-            float r[EPV];
+            for (int k = 0; k < W; ++k) {
+              float r[E::kPerWord];
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              float x[NS];
+              for (int l = 0; l < E::kPerWord; ++l) {
+                float x[NS];
 #pragma unroll
-              for (int q = 0; q < NS; ++q) x[q] = f[q][e];
-              r[e] = reduce_lane<NS, RED, FAST>(x, a.mean_div);
+                for (int q = 0; q < NS; ++q) x[q] = E::lane(v[u][q].w[k], l);
+                r[l] = reduce_lane<NS, RED, FAST>(x, a.mean_div);
+              }
+              out.w[k] = E::pack_word(r);
             }
-            out = E::template pack<W>(r);
           }
           for (int d = 0; d < ndst; ++d)
             st_vec<W>(static_cast<char*>(sv.dst(d, EB)) + idx * VB, out);
@@ -436,6 +445,158 @@ inline int resident_blocks(const void* fn) {
   return per_sm;
 }
 
+// ---- bulk-copy (TMA) pass for the pure copies ------------------------------------
+// broadcast, all_gather, the list all_gather and all_to_all move bytes only.
+// Here one elected thread per CTA streams tiles through shared memory with the
+// bulk-copy engine: cp.async.bulk loads a tile (completion counted on an
+// mbarrier) and cp.async.bulk stores the same tile to every destination, so
+// the data never passes through registers.  Requires 16-byte aligned
+// addresses and a segment length that is a multiple of 16 bytes (the host
+// checks; otherwise the vector pass runs).  Every mbarrier wait is bounded:
+// if a tile never arrives the CTA raises its timeout flag, drains its stores
+// and returns.
+#ifndef RCC_BULK_TILE
+#define RCC_BULK_TILE 16384
+#endif
+#ifndef RCC_BULK_STAGES
+#define RCC_BULK_STAGES 4
+#endif
+#ifndef RCC_BULK_COPY
+#define RCC_BULK_COPY 0
+#endif
+constexpr int kBulkTile = RCC_BULK_TILE;
+constexpr int kBulkStages = RCC_BULK_STAGES;
+constexpr uint32_t kBulkSpinLimit = 1u << 24;
+
+// raised (never cleared on the device) when a bounded wait gave up
+static __device__ uint32_t g_bulk_timeout;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+template <int EB>
+__global__ void __launch_bounds__(32) bulk_copy_kernel(const __grid_constant__ MultiPtrArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bars[kBulkStages];
+  if (threadIdx.x != 0) return;
+  const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
+                   (size_t)blockIdx.y * a.dst_seg_stride};
+  const int ndst = sv.ndst();
+  const char* src = static_cast<const char*>(sv.src(0, EB));
+  const size_t bytes = a.n * (size_t)EB;  // multiple of 16 (host-checked)
+  const size_t ntiles = (bytes + kBulkTile - 1) / kBulkTile;
+  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const size_t mine = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  for (int s = 0; s < kBulkStages; ++s)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[s])) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+  auto tile_bytes = [&](size_t t) -> uint32_t {
+    const size_t off = t * (size_t)kBulkTile;
+    const size_t left = bytes - off;
+    return (uint32_t)(left < (size_t)kBulkTile ? left : (size_t)kBulkTile);
+  };
+  auto issue_load = [&](size_t j) {  // j-th tile of this CTA into stage j % S
+    const size_t t = blockIdx.x + j * gridDim.x;
+    const int s = (int)(j % kBulkStages);
+    const uint32_t nb = tile_bytes(t);
+    const uint32_t bar = smem_u32(&bars[s]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(nb)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(smem + (size_t)s * kBulkTile)),
+        "l"(src + t * (size_t)kBulkTile), "r"(nb), "r"(bar)
+        : "memory");
+  };
+
+  const size_t prologue = mine < (size_t)kBulkStages ? mine : (size_t)kBulkStages;
+  for (size_t j = 0; j < prologue; ++j) issue_load(j);
+  bool timed_out = false;
+  for (size_t j = 0; j < mine; ++j) {
+    const int s = (int)(j % kBulkStages);
+    const uint32_t parity = (uint32_t)((j / kBulkStages) & 1);
+    const uint32_t bar = smem_u32(&bars[s]);
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+      if (++spins >= kBulkSpinLimit) {
+        timed_out = true;
+        break;
+      }
+    }
+    if (timed_out) break;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const size_t t = blockIdx.x + j * gridDim.x;
+    const uint32_t nb = tile_bytes(t);
+    const uint32_t from = smem_u32(smem + (size_t)s * kBulkTile);
+    for (int d = 0; d < ndst; ++d) {
+      char* dst = static_cast<char*>(sv.dst(d, EB)) + t * (size_t)kBulkTile;
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                   "r"(from), "r"(nb)
+                   : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    if (j + kBulkStages < mine) {
+      // the stage is refilled only after its stores have read it
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      issue_load(j + kBulkStages);
+    }
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (timed_out) {
+    atomicExch(&g_bulk_timeout, 1u);
+    // let every load still in flight land before the CTA's shared memory goes
+    for (size_t j = 0; j < mine && j < (size_t)kBulkStages; ++j) {
+      const uint32_t bar = smem_u32(&bars[j % kBulkStages]);
+      for (uint32_t spins = 0; spins < kBulkSpinLimit; ++spins)
+        if (mbar_try_wait(bar, 0) || mbar_try_wait(bar, 1)) break;
+    }
+  }
+}
+
+template <int EB>
+cudaError_t launch_bulk_copy(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+  const size_t smem = (size_t)kBulkStages * kBulkTile;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(bulk_copy_kernel<EB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const size_t ntiles = (a.n * (size_t)EB + kBulkTile - 1) / kBulkTile;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bulk_copy_kernel<EB>, 32, smem);
+  if (per_sm < 1) per_sm = 1;
+  size_t cap = (size_t)per_sm * sm_count() / (size_t)nseg;
+  if (cap < 1) cap = 1;
+  const unsigned gx = (unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap);
+  bulk_copy_kernel<EB><<<dim3(gx, (unsigned)nseg), 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// Reads and clears this translation unit's bulk-copy timeout flag.
+inline cudaError_t bulk_copy_timeouts(uint32_t* out) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_bulk_timeout, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_bulk_timeout, &zero, sizeof(uint32_t));
+  return e;
+}
+
 // Widest vector the addresses allow (RCC_VEC_BYTES=16 caps it at 16 bytes).
 inline int vec_cap() {
   static int cap = [] {
@@ -496,7 +657,10 @@ cudaError_t launch_typed(Red red, bool fast, int nseg, const MultiPtrArgs& a,
                   : launch_red<T, kRedSum, false>(nseg, a, stream);
     case kRedMax: return launch_red<T, kRedMax, false>(nseg, a, stream);
     case kRedMin: return launch_red<T, kRedMin, false>(nseg, a, stream);
-    case kRedCopy: return launch_ns<T, 1, kRedCopy, false>(nseg, a, stream);
+    case kRedCopy:
+      if (RCC_BULK_COPY && a.vec_ok >= 16 && (a.n * Elem<T>::kBytes) % 16 == 0)
+        return launch_bulk_copy<Elem<T>::kBytes>(nseg, a, stream);
+      return launch_ns<T, 1, kRedCopy, false>(nseg, a, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -7,4 +7,5 @@ cudaError_t launch_multi_ptr_bf16(Red red, bool fast, int nseg, const MultiPtrAr
                                   cudaStream_t stream) {
   return mp::launch_typed<__nv_bfloat16>(red, fast, nseg, a, stream);
 }
+cudaError_t bulk_copy_timeouts_bf16(uint32_t* out) { return mp::bulk_copy_timeouts(out); }
 }  // namespace rcc

@@ -486,6 +486,11 @@ rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream) {
   }
   unregister(comm);
   wake_waiters(*s);
+  // a bulk-copy CTA that gave up waiting leaves its flag raised
+  uint32_t f32 = 0, bf16 = 0;
+  if (rcc::bulk_copy_timeouts_f32(&f32) == cudaSuccess &&
+      rcc::bulk_copy_timeouts_bf16(&bf16) == cudaSuccess && (f32 | bf16))
+    return fail(RCC_ERR_TIMEOUT, "a bulk-copy wait gave up: some copy output is incomplete");
   return RCC_OK;
 }
 

@@ -52,6 +52,9 @@ cudaError_t launch_multi_ptr_f32(Red red, bool fast, int nseg, const MultiPtrArg
                                  cudaStream_t stream);
 cudaError_t launch_multi_ptr_bf16(Red red, bool fast, int nseg, const MultiPtrArgs& a,
                                   cudaStream_t stream);
+// Read and clear the flag a bulk-copy CTA raises when a bounded wait gave up.
+cudaError_t bulk_copy_timeouts_f32(uint32_t* out);
+cudaError_t bulk_copy_timeouts_bf16(uint32_t* out);
 
 // ---- gradient sync -------------------------------------------------------
 
