@@ -77,7 +77,7 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="size sweep: all_reduce mean (fp32, bf16), broadcast root 0 and reduce "
                          "root R-1 for R in {2,4,8}, N = 257*4^k and 2^28; one JSON line per point")
-    ap.add_argument("--gs-mode", default="host", choices=["host", "device", "graph"],
+    ap.add_argument("--gs-mode", default="host", choices=["host", "device", "graph", "multi"],
                     help="grad-sync decision: host readback (default), device kernel, or device "
                          "kernel + captured update launches")
     return ap.parse_args()
@@ -517,7 +517,8 @@ def bench_grad_sync_1024(args):
                             exp_avg_sq=[torch.zeros(n, device=dev) for _ in range(rep)],
                             mean_grad=torch.empty(n, device=dev)))
     sets = rcc.ParamSets(tensors)
-    flags = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH}[args.gs_mode]
+    flags = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
+             "multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR}[args.gs_mode]
     cfg = rcc.adamw_cfg(replicas=rep, flags=flags)
     state = rcc.optim_state(scale=65536.0)
     h = rcc.register(0, Rk, rcc.F32, True)

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constan
 
   SqAcc acc;
   uint64_t scalar_from = c0;
-  if (t.vec_ok) {
+  if (t.vec_ok & 1u) {
     // c0 is a multiple of 4 (elems_per_row is), so vectors start aligned
     const uint64_t v0 = c0 / 4, v1 = c1 / 4;
     scalar_from = v1 * 4;
@@ -243,108 +243,176 @@ __device__ __forceinline__ void adamw_elem(float g, const AdamWScalars& s, float
   v = vi;
 }
 
-// ptr table layout of one tensor: params[0..rep), exp_avg[0..rep), exp_avg_sq[0..rep)
-template <int REP>  // REP > 0: compile-time replica count; 0: runtime
-__global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
-  const int rep = REP > 0 ? REP : a.replicas;
-  float* const* P = a.state;
-  // With a device decision, the skip flag, the clip coefficient, the step
-  // scalars and the inverse loss scale come from device memory.  They are
-  // fetched first but examined only after this thread's first loads are in
-  // flight, so their latency overlaps the data instead of preceding it.
+// ---- the update body shared by the per-tensor and multi-tensor kernels ----
+// P: one tensor's state pointer table, params[0..rep), exp_avg[0..rep),
+// exp_avg_sq[0..rep).  The gradient is the stored mean gradient, or it is
+// recomputed from the R scaled gradients with the statistics kernel's
+// arithmetic.
+
+// The decision source: host values in the launch arguments, or (with a
+// device decision) the skip flag, coefficient, scalars and inverse scale in
+// device memory.  Fetched first, examined only after the first data loads are
+// in flight.
+struct StepView {
   GsDecision d;
-  d.skip = 0u;
-  d.coef = a.clip_coef;
-  AdamWScalars sc = a.s;
-  float inv_scale = a.inv_scale;
-  if (a.decision) {
-    d = *a.decision;
-    sc = *a.dev_scalars;
-    inv_scale = sc.inv_scale;
+  AdamWScalars sc;
+  float inv_scale;
+};
+
+__device__ __forceinline__ StepView step_view(float clip, const AdamWScalars& s, float inv_scale,
+                                            const GsDecision* decision,
+                                            const AdamWScalars* dev_scalars) {
+  StepView v;
+  v.d.skip = 0u;
+  v.d.coef = clip;
+  v.sc = s;
+  v.inv_scale = inv_scale;
+  if (decision) {
+    v.d = *decision;
+    v.sc = *dev_scalars;
+    v.inv_scale = v.sc.inv_scale;
   }
+  return v;
+}
+
+// Elements [4v, 4v+4) of one tensor.  Returns false (having written nothing)
+// when the step is skipped.
+template <int REP>
+__device__ __forceinline__ bool update_vec4(float* const* P, int rep, const float* mean_grad,
+                                            const float* const* grads, int R, uint64_t v,
+                                            const StepView& sv) {
   constexpr int RB = REP > 0 ? REP : 4;  // replicas per batch of loads
-  const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
-  const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-  const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
-  for (uint64_t v = tid; v < nv; v += nthreads) {
-    // the gradient inputs and the first batch of state, all in flight together
-    float4 g4;
-    if (a.mean_grad) {
-      const uint4 x = ld_vec(a.mean_grad + v * 4);
-      g4 = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
-                       __uint_as_float(x.w));
-    } else {
-      g4 = *reinterpret_cast<const float4*>(a.grads[0] + v * 4);
-      for (int q = 1; q < a.R; ++q) {
-        const float4 y = *reinterpret_cast<const float4*>(a.grads[q] + v * 4);
-        g4.x = __fadd_rn(g4.x, y.x);
-        g4.y = __fadd_rn(g4.y, y.y);
-        g4.z = __fadd_rn(g4.z, y.z);
-        g4.w = __fadd_rn(g4.w, y.w);
-      }
+  // the gradient inputs and the first batch of state, all in flight together
+  float4 g4;
+  if (mean_grad) {
+    const uint4 x = ld_vec(mean_grad + v * 4);
+    g4 = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                     __uint_as_float(x.w));
+  } else {
+    g4 = *reinterpret_cast<const float4*>(grads[0] + v * 4);
+    for (int q = 1; q < R; ++q) {
+      const float4 y = *reinterpret_cast<const float4*>(grads[q] + v * 4);
+      g4.x = __fadd_rn(g4.x, y.x);
+      g4.y = __fadd_rn(g4.y, y.y);
+      g4.z = __fadd_rn(g4.z, y.z);
+      g4.w = __fadd_rn(g4.w, y.w);
     }
-    float4 p[RB], m[RB], w[RB];
+  }
+  float4 p[RB], m[RB], w[RB];
 #pragma unroll
-    for (int k = 0; k < RB; ++k) {
-      if (k < rep) {
-        p[k] = ld_state(P[k] + v * 4);
-        m[k] = ld_state(P[rep + k] + v * 4);
-        w[k] = ld_state(P[2 * rep + k] + v * 4);
-      }
+  for (int k = 0; k < RB; ++k) {
+    if (k < rep) {
+      p[k] = ld_state(P[k] + v * 4);
+      m[k] = ld_state(P[rep + k] + v * 4);
+      w[k] = ld_state(P[2 * rep + k] + v * 4);
     }
-    if (d.skip) return;  // skipped step: state untouched
-    float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-    if (!a.mean_grad) {
-      const float Rf = (float)a.R;
+  }
+  if (sv.d.skip) return false;  // skipped step: state untouched
+  float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+  if (!mean_grad) {
+    const float Rf = (float)R;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(__fdiv_rn(gv[e], Rf), inv_scale);
-    }
+    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(__fdiv_rn(gv[e], Rf), sv.inv_scale);
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], d.coef);
-    for (int r0 = 0; r0 < rep; r0 += RB) {
-      if (r0 > 0) {
-#pragma unroll
-        for (int k = 0; k < RB; ++k) {
-          if (r0 + k < rep) {
-            p[k] = ld_state(P[r0 + k] + v * 4);
-            m[k] = ld_state(P[rep + r0 + k] + v * 4);
-            w[k] = ld_state(P[2 * rep + r0 + k] + v * 4);
-          }
-        }
-      }
+  for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], sv.d.coef);
+  for (int r0 = 0; r0 < rep; r0 += RB) {
+    if (r0 > 0) {
 #pragma unroll
       for (int k = 0; k < RB; ++k) {
         if (r0 + k < rep) {
-          adamw_elem(gv[0], sc, p[k].x, m[k].x, w[k].x);
-          adamw_elem(gv[1], sc, p[k].y, m[k].y, w[k].y);
-          adamw_elem(gv[2], sc, p[k].z, m[k].z, w[k].z);
-          adamw_elem(gv[3], sc, p[k].w, m[k].w, w[k].w);
-          *reinterpret_cast<float4*>(P[r0 + k] + v * 4) = p[k];
-          *reinterpret_cast<float4*>(P[rep + r0 + k] + v * 4) = m[k];
-          *reinterpret_cast<float4*>(P[2 * rep + r0 + k] + v * 4) = w[k];
+          p[k] = ld_state(P[r0 + k] + v * 4);
+          m[k] = ld_state(P[rep + r0 + k] + v * 4);
+          w[k] = ld_state(P[2 * rep + r0 + k] + v * 4);
         }
       }
     }
-  }
-  if (d.skip) return;
-  for (uint64_t i = nv * 4 + tid; i < a.numel; i += nthreads) {
-    float g;
-    if (a.mean_grad) {
-      g = a.mean_grad[i];
-    } else {
-      float s = a.grads[0][i];
-      for (int q = 1; q < a.R; ++q) s = __fadd_rn(s, a.grads[q][i]);
-      g = __fmul_rn(__fdiv_rn(s, (float)a.R), inv_scale);
-    }
-    g = __fmul_rn(g, d.coef);
-    for (int r = 0; r < rep; ++r) {
-      float p = P[r][i], m = P[rep + r][i], w = P[2 * rep + r][i];
-      adamw_elem(g, sc, p, m, w);
-      P[r][i] = p;
-      P[rep + r][i] = m;
-      P[2 * rep + r][i] = w;
+#pragma unroll
+    for (int k = 0; k < RB; ++k) {
+      if (r0 + k < rep) {
+        adamw_elem(gv[0], sv.sc, p[k].x, m[k].x, w[k].x);
+        adamw_elem(gv[1], sv.sc, p[k].y, m[k].y, w[k].y);
+        adamw_elem(gv[2], sv.sc, p[k].z, m[k].z, w[k].z);
+        adamw_elem(gv[3], sv.sc, p[k].w, m[k].w, w[k].w);
+        *reinterpret_cast<float4*>(P[r0 + k] + v * 4) = p[k];
+        *reinterpret_cast<float4*>(P[rep + r0 + k] + v * 4) = m[k];
+        *reinterpret_cast<float4*>(P[2 * rep + r0 + k] + v * 4) = w[k];
+      }
     }
   }
+  return true;
+}
+
+// One element of one tensor (ragged tails and unaligned tensors); the caller
+// has already checked the skip flag.
+__device__ __forceinline__ void update_one(float* const* P, int rep, const float* mean_grad,
+                                           const float* const* grads, int R, uint64_t i,
+                                           const StepView& sv) {
+  float g;
+  if (mean_grad) {
+    g = mean_grad[i];
+  } else {
+    float s = grads[0][i];
+    for (int q = 1; q < R; ++q) s = __fadd_rn(s, grads[q][i]);
+    g = __fmul_rn(__fdiv_rn(s, (float)R), sv.inv_scale);
+  }
+  g = __fmul_rn(g, sv.d.coef);
+  for (int r = 0; r < rep; ++r) {
+    float p = P[r][i], m = P[rep + r][i], w = P[2 * rep + r][i];
+    adamw_elem(g, sv.sc, p, m, w);
+    P[r][i] = p;
+    P[rep + r][i] = m;
+    P[2 * rep + r][i] = w;
+  }
+}
+
+// One launch per tensor (the pages' design).
+template <int REP>  // REP > 0: compile-time replica count; 0: runtime
+__global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
+  const int rep = REP > 0 ? REP : a.replicas;
+  const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
+  const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
+  const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+  const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
+  for (uint64_t v = tid; v < nv; v += nthreads)
+    if (!update_vec4<REP>(a.state, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
+  if (sv.d.skip) return;
+  for (uint64_t i = nv * 4 + tid; i < a.numel; i += nthreads)
+    update_one(a.state, rep, a.mean_grad, a.grads, a.R, i, sv);
+}
+
+// One launch for every tensor: block b updates statistics row b (a chunk of
+// elems_per_row elements of one tensor), the statistics kernel's partition.
+template <int REP>
+__global__ void __launch_bounds__(kThreads)
+    gs_update_multi_kernel(const __grid_constant__ GsMultiUpdateArgs a) {
+  const int rep = REP > 0 ? REP : a.replicas;
+  const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
+  const uint64_t row = blockIdx.x;
+  uint32_t lo = 0, hi = a.num_tensors - 1;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi + 1) >> 1;
+    if (a.tensors[mid].row_begin <= row)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const GsTensor t = a.tensors[lo];
+  float* const* P = a.state + (size_t)lo * 3 * rep;
+  const float* const* g = a.grads + t.grad_slot;
+  const uint64_t c0 = (row - t.row_begin) * (uint64_t)a.elems_per_row;
+  uint64_t c1 = c0 + a.elems_per_row;
+  if (c1 > t.numel) c1 = t.numel;
+  uint64_t scalar_from = c0;
+  if (t.vec_ok & 2u) {
+    const uint64_t v1 = c1 / 4;
+    scalar_from = v1 * 4;
+    for (uint64_t v = c0 / 4 + threadIdx.x; v < v1; v += kThreads)
+      if (!update_vec4<REP>(P, rep, t.mean_grad, g, a.R, v, sv)) return;
+  }
+  if (sv.d.skip) return;
+  for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads)
+    update_one(P, rep, t.mean_grad, g, a.R, i, sv);
 }
 
 // The decision the host would take from the report: skip on any non-finite
@@ -401,6 +469,19 @@ cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
                              cudaStream_t stream) {
   gs::gs_report_kernel<<<1, kThreads, 0, stream>>>(in, nrows, report);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gs_update_multi(const GsMultiUpdateArgs& a, cudaStream_t stream) {
+  if (a.total_rows == 0) return cudaSuccess;
+  const dim3 grid((unsigned)a.total_rows);
+  switch (a.replicas) {
+    case 1: gs::gs_update_multi_kernel<1><<<grid, kThreads, 0, stream>>>(a); break;
+    case 2: gs::gs_update_multi_kernel<2><<<grid, kThreads, 0, stream>>>(a); break;
+    case 4: gs::gs_update_multi_kernel<4><<<grid, kThreads, 0, stream>>>(a); break;
+    case 8: gs::gs_update_multi_kernel<8><<<grid, kThreads, 0, stream>>>(a); break;
+    default: gs::gs_update_multi_kernel<0><<<grid, kThreads, 0, stream>>>(a); break;
+  }
   return cudaGetLastError();
 }
 

@@ -1128,8 +1128,11 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return fail(RCC_ERR_INVALID_ARGUMENT, "gradient sync needs an RCC_F32 session");
   if (rep != 1 && rep != R)
     return fail(RCC_ERR_INVALID_ARGUMENT, "replicas %d must be 1 or %d", rep, R);
-  if (cfg->flags & ~(RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH))
+  if (cfg->flags & ~(RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH | RCC_ADAMW_MULTI_TENSOR))
     return fail(RCC_ERR_INVALID_ARGUMENT, "unknown cfg->flags bits 0x%x", cfg->flags);
+  if ((cfg->flags & RCC_ADAMW_GRAPH) && (cfg->flags & RCC_ADAMW_MULTI_TENSOR))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "RCC_ADAMW_GRAPH and RCC_ADAMW_MULTI_TENSOR exclude "
+                                          "each other (the multi-tensor update is one launch)");
   if (!finite_pos(cfg->lr) && cfg->lr != 0.0)
     return fail(RCC_ERR_INVALID_ARGUMENT, "lr must be finite and >= 0");
   if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
@@ -1201,14 +1204,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       gtab[p * R + r] = ps.grads[r];
       gv = gv && aligned16(ps.grads[r]);
     }
-    rcc::GsTensor t{};
-    t.numel = ps.numel;
-    t.row_begin = row;
-    t.mean_grad = ps.mean_grad;
-    t.grad_slot = (uint32_t)(p * R);
-    t.vec_ok = gv ? 1u : 0u;
-    tens[p] = t;
-    row += (ps.numel + epr - 1) / epr;
     bool uv = gv;
     for (int k = 0; k < rep; ++k) {
       stab[p * 3 * rep + k] = ps.params[k];
@@ -1217,6 +1212,14 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       uv = uv && aligned16(ps.params[k]) && aligned16(ps.exp_avg[k]) && aligned16(ps.exp_avg_sq[k]);
     }
     upd_vec[p] = uv ? 1 : 0;
+    rcc::GsTensor t{};
+    t.numel = ps.numel;
+    t.row_begin = row;
+    t.mean_grad = ps.mean_grad;
+    t.grad_slot = (uint32_t)(p * R);
+    t.vec_ok = (gv ? 1u : 0u) | (uv ? 2u : 0u);
+    tens[p] = t;
+    row += (ps.numel + epr - 1) / epr;
   }
   // the previous call's update kernels may still read the tables
   cudaError_t e;
@@ -1360,6 +1363,26 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return cudaSuccess;
   };
 
+  const bool multi = (cfg->flags & RCC_ADAMW_MULTI_TENSOR) != 0;
+  auto enqueue_multi = [&](cudaStream_t where) -> cudaError_t {
+    rcc::GsMultiUpdateArgs ma{};
+    ma.tensors = reinterpret_cast<const rcc::GsTensor*>(dbase);
+    ma.grads = reinterpret_cast<const float* const*>(dbase + off_grads);
+    ma.state = reinterpret_cast<float* const*>(dbase + off_state);
+    ma.total_rows = total_rows;
+    ma.num_tensors = (uint32_t)P;
+    ma.elems_per_row = epr;
+    ma.R = R;
+    ma.replicas = rep;
+    ma.inv_scale = ua.inv_scale;
+    ma.clip_coef = ua.clip_coef;
+    ma.s = ua.s;
+    ma.decision = ua.decision;
+    ma.dev_scalars = ua.dev_scalars;
+    return rcc::launch_gs_update_multi(ma, where);
+  };
+  const uint64_t launches_per_update = multi ? 1 : P;
+
   uint64_t device_updates = 0;
   if (on_device) {
     // decide on the GPU and enqueue the updates behind it, before waiting
@@ -1398,10 +1421,11 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       if ((e = cudaGraphLaunch(sc.graph_exec, cs)) != cudaSuccess)
         return cuda_fail(e, "cudaGraphLaunch");
     } else {
-      if ((e = enqueue_branched(cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
+      if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess)
+        return cuda_fail(e, "update kernel");
     }
-    device_updates = P;
-    g_launches.fetch_add(P, std::memory_order_relaxed);
+    device_updates = launches_per_update;
+    g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
   }
   if ((st = wait_event(sc.report_ev, "12-byte report readback")) != RCC_OK) return st;
 
@@ -1442,9 +1466,10 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     const int64_t t = t_next;
     ua.s = step_scalars(cfg, t);
     ua.clip_coef = coef;
-    if ((e = enqueue_branched(cs)) != cudaSuccess) return cuda_fail(e, "update kernel");
-    g_launches.fetch_add(P, std::memory_order_relaxed);
-    rep_out.update_launches = P;
+    if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess)
+      return cuda_fail(e, "update kernel");
+    g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
+    rep_out.update_launches = launches_per_update;
     state->step = t;
     state->growth_tracker += 1;
     if (state->growth_tracker >= state->growth_interval) {

@@ -64,7 +64,8 @@ struct GsTensor {
   uint64_t row_begin;       // first statistics row of this tensor
   float* mean_grad;         // optional output of the unscaled mean gradient
   uint32_t grad_slot;       // index of this tensor's R grad pointers in the grad table
-  uint32_t vec_ok;          // all R grads (and mean_grad) 16-byte aligned
+  uint32_t vec_ok;          // bit 0: all R grads (and mean_grad) 16-byte aligned;
+                            // bit 1: so are all its state pointers (update vectors)
 };
 
 struct GsStatsArgs {
@@ -119,6 +120,25 @@ struct GsUpdateArgs {
 };
 
 cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream);
+
+// Every tensor's update in one launch (a comparison point for the one
+// kernel per parameter the pages describe): block b updates statistics row b.
+struct GsMultiUpdateArgs {
+  const GsTensor* tensors;      // [num_tensors]
+  const float* const* grads;    // grad pointer table
+  float* const* state;          // state table: tensor p at p * 3 * replicas
+  uint64_t total_rows;
+  uint32_t num_tensors;
+  uint32_t elems_per_row;
+  int R;
+  int replicas;
+  float inv_scale;
+  float clip_coef;
+  AdamWScalars s;
+  const GsDecision* decision;
+  const AdamWScalars* dev_scalars;
+};
+cudaError_t launch_gs_update_multi(const GsMultiUpdateArgs& a, cudaStream_t stream);
 // One thread turns the 12-byte report into the decision (same arithmetic as the host).
 cudaError_t launch_gs_decide(const uint32_t* report, double max_grad_norm, GsDecision* out,
                              cudaStream_t stream);

@@ -34,6 +34,7 @@ OPS = {"sum": SUM, "mean": MEAN, "max": MAX, "min": MIN}
 DETERMINISTIC = 0x1
 ADAMW_DEVICE_DECISION = 0x1
 ADAMW_GRAPH = 0x2
+ADAMW_MULTI_TENSOR = 0x4
 MAX_RANKS = 64
 
 # every symbol include/rcc.h declares

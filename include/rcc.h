@@ -176,7 +176,8 @@ rcc_status rcc_all_gather_list(rcc_comm comm, const void* const* send,
                                rcc_stream_t stream);
 
 /* ---- per-rank arrival ------------------------------------------------------
- * [ruCCL §1, §7 (in_process: logical ranks inside one process), §3: every
+ * [ruCCL introduction and §1 (the in_process implementation: logical ranks
+ * inside one process), §3: every
  * rank calls matching collectives in the same order with matching shape, op
  * and root; Monarch Communicator::new: one thread per rank].
  * Each logical rank -- typically its own host thread -- calls the *_rank form
@@ -244,9 +245,13 @@ typedef struct {
  *   report is still read back before the call returns.
  * RCC_ADAMW_GRAPH: as DEVICE_DECISION, and the per-tensor update launches are
  *   captured once into a CUDA graph and replayed while the tensors' pointers
- *   and sizes stay the same (still one kernel node per parameter tensor). */
+ *   and sizes stay the same (still one kernel node per parameter tensor).
+ * RCC_ADAMW_MULTI_TENSOR: one update launch covers every tensor (one CTA per
+ *   statistics row) instead of one launch per tensor -- a comparison point
+ *   against the pages' one-kernel-per-parameter design; not with GRAPH. */
 #define RCC_ADAMW_DEVICE_DECISION 0x1u
 #define RCC_ADAMW_GRAPH 0x2u
+#define RCC_ADAMW_MULTI_TENSOR 0x4u
 
 /* Optimizer step count and GradScaler state, owned by the caller, updated by
  * each call ([RUDA-T]: scale -> step -> update on the same GradScaler). */
@@ -288,9 +293,13 @@ typedef struct {
  *      replica: p = p*(1 - lr*wd); m = b1*m + (1-b1)*g'; v = b2*v + (1-b2)*g'^2;
  *      p -= lr/(1-b1^t) * m / (sqrt(v)/sqrt(1-b2^t) + eps), g' = g*clip_coef;
  *      S grows after growth_interval finite steps.
- * Session dtype must be RCC_F32.  Gradients are never written.  `state` is
- * read and updated; `report` (may be NULL) receives what happened.  Returns
- * RCC_ERR_TIMEOUT if the report did not arrive within the wait limit. */
+ * Session dtype must be RCC_F32.  Gradients are never written (several ranks
+ * or tensors may even share one gradient buffer).  The update kernels of
+ * different tensors may run concurrently, so parameter, moment and
+ * mean-gradient buffers must not overlap any other buffer of the call
+ * (RCC_ERR_INVALID_ARGUMENT; checked whenever the set of buffers changes).
+ * `state` is read and updated; `report` (may be NULL) receives what happened.
+ * Returns RCC_ERR_TIMEOUT if the report did not arrive within the wait limit. */
 rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params,
                                int num_params, const rcc_adamw_cfg* cfg,
                                rcc_optim_state* state, rcc_step_report* report,

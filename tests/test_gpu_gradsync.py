@@ -99,9 +99,11 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
                 want = orc.stats_value(st)
                 assert abs(rep.sum_sq - want) <= 1e-12 * want, (rep.sum_sq, want)
                 assert abs(rep.clip_coef - d.clip_coef) <= 2e-7 * d.clip_coef
-                assert rep.update_launches == len(prob.sizes)
+                per = 1 if cfg.flags & rcc.ADAMW_MULTI_TENSOR else len(prob.sizes)
+                assert rep.update_launches == per
             else:   # the host flow launches nothing; the device flow's updates return at once
-                assert rep.update_launches == (0 if cfg.flags == 0 else len(prob.sizes))
+                per = 1 if cfg.flags & rcc.ADAMW_MULTI_TENSOR else len(prob.sizes)
+                assert rep.update_launches == (per if cfg.flags & rcc.ADAMW_DEVICE_DECISION else 0)
             if check_each or k == steps:
                 for i in range(len(prob.sizes)):
                     t = prob.tensors[i]
@@ -115,7 +117,9 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
     return reports, state
 
 
-MODES = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH}
+MODES = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
+         "multi": rcc.ADAMW_MULTI_TENSOR,
+         "device_multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR}
 
 
 @pytest.mark.parametrize("mode", list(MODES))
@@ -150,7 +154,7 @@ def test_decision_modes_bitwise_identical():
         assert state.step == 5
         finals[mode] = [torch.cat([t["params"][1], t["exp_avg"][0], t["exp_avg_sq"][1]]).cpu()
                         for t in prob.tensors]
-    for mode in ("device", "graph"):
+    for mode in ("device", "graph", "multi", "device_multi"):
         for a, b in zip(finals["host"], finals[mode]):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32)), mode
 

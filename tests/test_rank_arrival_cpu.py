@@ -1,8 +1,9 @@
 """Per-rank arrival on the host (no GPU): each logical rank is its own thread.
 
-[ruCCL README §1/§7: the in_process implementation runs logical ranks inside
-one process; §3: every rank calls matching collectives in the same order with
-matching shape, op and root; §4: reset discards in-flight operation state.]
+[ruCCL README introduction and §1: the in_process implementation runs logical
+ranks inside one process; §3: every rank calls matching collectives in the
+same order with matching shape, op and root; §4: reset discards in-flight
+operation state.]
 The last rank to arrive checks the set and launches; every rank returns the
 same status.  Sessions are registered on device ordinal 63 (never current),
 so an agreeing set stops at the device check and launches nothing; the fake
