@@ -103,7 +103,8 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
                 assert rep.update_launches == per
             else:   # the host flow launches nothing; the device flow's updates return at once
                 per = 1 if cfg.flags & rcc.ADAMW_MULTI_TENSOR else len(prob.sizes)
-                assert rep.update_launches == (per if cfg.flags & rcc.ADAMW_DEVICE_DECISION else 0)
+                on_device = cfg.flags & (rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_GRAPH)
+                assert rep.update_launches == (per if on_device else 0)
             if check_each or k == steps:
                 for i in range(len(prob.sizes)):
                     t = prob.tensors[i]
