@@ -19,7 +19,8 @@ NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["collectives_f32.cu", "collectives_bf16.cu", "gradsync.cu", "rcc_host.cpp"]
+SOURCES = ["collectives_f32.cu", "collectives_bf16.cu", "gradsync.cu", "rcc_host.cpp",
+           "rcc_rank.cpp", "rcc_gradsync_host.cpp"]
 
 
 def _inputs():
