@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -53,13 +54,14 @@ MIN_TRAFFIC = {
 }
 METRIC = "all_reduce algorithm GB/s and % of GB300 HBM roofline vs R, N, dtype (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0        # HBM3e data-sheet figure, for context only
 WORKLOAD = "8 ranks x 2^24 fp32 per rank, gradient-like N(0,1e-2) + 0.1% x100"
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -126,8 +128,11 @@ def peak_hbm():
         with open(path) as f:
             d = json.load(f)
         for key in ("hbm_gbs", "hbm_GBs", "hbm"):
-            if key in d and isinstance(d[key], (int, float)):
-                return float(d[key]), "measured"
+            v = d.get(key)
+            if isinstance(v, dict):     # {"burst": ..., ...}: a kernel timed alone
+                v = v.get("burst", v.get("value"))
+            if isinstance(v, (int, float)) and v > 0:
+                return float(v), "measured"
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback"
@@ -171,12 +176,22 @@ class ClockSampler:
             self.f = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def lines(self):
+        """Sample lines written so far (the file is shared with the child)."""
+        if self.f is None:
+            return 0
+        self.f.flush()
+        with open("/proc/self/fd/%d" % self.f.fileno()) as g:
+            return sum(1 for _ in g)
+
+    def stop(self, first_line=0):
+        """Summarise the samples from line `first_line` on (the timed region);
+        if that window holds none, the load pre-roll's samples stand in."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -185,9 +200,14 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.seek(0)
+        all_lines = self.f.read().splitlines()
+        window = "timed region"
+        chosen = all_lines[first_line:]
+        if not any(len(l.split(",")) >= 7 for l in chosen):
+            chosen, window = all_lines, "load pre-roll and timed region"
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.f:
+        for line in chosen:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -202,7 +222,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": window,
+                "interval_ms": 100}
 
 
 # ------------------------------------------------------------------ our arm
@@ -340,9 +361,17 @@ def bench_ours(args):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
               for _ in range(K)]
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # load pre-roll: keep stepping (untimed) until the clock sampler is up
         sampler = ClockSampler(local)
         sampler.start()
-        time.sleep(0.4)                 # let the sampler see the load from the first steps
+        t_pre = time.perf_counter()
+        while sampler.proc is not None and time.perf_counter() - t_pre < 3.0:
+            for _ in range(20):
+                wl.step(h)
+            torch.cuda.synchronize()
+            if sampler.lines() >= 2:
+                break
+        first_line = sampler.lines()
         launches0 = rcc.launch_count()
         barrier(world)
         torch.cuda.synchronize()
@@ -353,7 +382,7 @@ def bench_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         launches = rcc.launch_count() - launches0
-        clocks = sampler.stop()
+        clocks = sampler.stop(first_line)
         ms_total = start.elapsed_time(end)
         row_ms = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
                   for i, name in enumerate(ROWS)}
@@ -403,7 +432,7 @@ def bench_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": "all_reduce (multi-pointer pass, fp32, R=8, N=2^24)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s",
+                     "peak_source": peak_src, "nominal_peak": NOMINAL_HBM_GBS, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
                      "algorithmic_bytes_per_launch": ar_traffic,
                      "avg_launch_ms": round(ar_ms, 4)},
@@ -440,6 +469,29 @@ def oracle_step(orc, xs, state):
     state[4] = t
 
 
+def host_info():
+    """Host cores and CPU model, recorded beside every oracle timing."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.startswith("Model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model, "machine": platform.machine()}
+
+
 def _oracle_setup(n):
     import oracle as orc
     from gradient_sync_rcc_gb300 import synth
@@ -462,6 +514,7 @@ def cpu_baseline(target_s=10.0, n=1 << 22):
             break
     alg = R * n * ES * len(ROWS) * reps
     return {"value": round(alg / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host": host_info(),
             "sample": "the step's 8 rows over 8 ranks x 2^22 fp32 (1/4 of the workload), "
                       "%d passes, %.1f s single-threaded" % (reps, el)}
 
@@ -470,11 +523,17 @@ def bench_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    n = 1 << 20
+    # each step is a bounded sample: 2^20 elements per rank (1/16 of the
+    # workload) up to 250 steps, halved for each doubling of the step count
+    # beyond that, so the whole run stays near a minute of host time
+    K = args.steps
+    shift = 0
+    while shift < 4 and K > 250 << shift:
+        shift += 1
+    n = (1 << 20) >> shift
     orc, xs, state = _oracle_setup(n)
     for _ in range(max(args.warmup, 3)):
         oracle_step(orc, xs, state)
-    K = args.steps
     t0 = time.perf_counter()
     for _ in range(K):
         oracle_step(orc, xs, state)
@@ -489,11 +548,19 @@ def bench_reference(args):
                       "rows_per_step": ROWS, "mode": "deterministic rank order"},
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                             "kind": "oracle",
-                            "sample": "each step: the 8 rows over 8 ranks x 2^20 fp32 "
-                                      "(1/16 of the workload), single-threaded"},
+                            "host": host_info(),
+                            "sample": "each step: the 8 rows over 8 ranks x 2^%d fp32 "
+                                      "(1/%d of the workload), single-threaded"
+                                      % (20 - shift, 16 << shift)},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
+
+
+def gs_flags(rcc, mode):
+    """`--gs-mode` -> rcc_adamw_cfg.flags."""
+    return {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
+            "multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR}[mode]
 
 
 def bench_grad_sync_1024(args):
@@ -517,9 +584,7 @@ def bench_grad_sync_1024(args):
                             exp_avg_sq=[torch.zeros(n, device=dev) for _ in range(rep)],
                             mean_grad=torch.empty(n, device=dev)))
     sets = rcc.ParamSets(tensors)
-    flags = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
-             "multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR}[args.gs_mode]
-    cfg = rcc.adamw_cfg(replicas=rep, flags=flags)
+    cfg = rcc.adamw_cfg(replicas=rep, flags=gs_flags(rcc, args.gs_mode))
     state = rcc.optim_state(scale=65536.0)
     h = rcc.register(0, Rk, rcc.F32, True)
     try:
@@ -542,12 +607,53 @@ def bench_grad_sync_1024(args):
         rcc.finish(h)
     traffic = (Rk * 4 + 4) * E + (4 + 24 * rep) * E
     peak, src = peak_hbm()
-    print(json.dumps({"case": "grad_sync_1024", "mode": args.gs_mode, "ranks": Rk, "tensors": P,
-                      "elements": E, "replicas": rep, "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall, 3),
-                      "launches_per_step": launches, "combine_launches": rep_.combine_launches,
-                      "min_traffic_bytes": traffic,
-                      "traffic_gbs": round(traffic / (ms * 1e-3) / 1e9, 1),
-                      "frac_of_" + src: round(traffic / (ms * 1e-3) / 1e9 / peak, 4)}), flush=True)
+    out = {"case": "grad_sync_1024", "mode": args.gs_mode, "ranks": Rk, "tensors": P,
+           "elements": E, "replicas": rep, "ms_per_step": round(ms, 3),
+           "wall_ms_per_step": round(wall, 3),
+           "launches_per_step": launches, "combine_launches": rep_.combine_launches,
+           "min_traffic_bytes": traffic,
+           "traffic_gbs": round(traffic / (ms * 1e-3) / 1e9, 1),
+           "frac_of_" + src: round(traffic / (ms * 1e-3) / 1e9 / peak, 4)}
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_grad_sync_sample(tensors, sizes, Rk, rep, E)
+    print(json.dumps(out), flush=True)
+
+
+def oracle_grad_sync_sample(tensors, sizes, Rk, rep, E):
+    """The oracle's step on this workload, streamed per tensor on host copies of
+    a sample of the tensors (the first ones, at least 2^25 elements), scaled to
+    the whole step by element count."""
+    import oracle as orc
+    orc.build.build()
+    n_s, host = 0, []
+    for i, n in enumerate(sizes):
+        host.append(([t.cpu().numpy() for t in tensors[i]["grads"]],
+                     tensors[i]["params"][0].cpu().numpy().copy(),
+                     np.zeros(n, np.float32), np.zeros(n, np.float32)))
+        n_s += n
+        if n_s >= 1 << 25:
+            break
+    inv = np.float32(1.0 / 65536.0)
+    t0 = time.perf_counter()
+    st = orc.stats_new()
+    means = []
+    for g, _, _, _ in host:
+        mean = orc.mean_unscale(g, inv)
+        orc.stats_accumulate(st, mean)
+        means.append(mean)
+    d = orc.decide(st, 1.0)
+    s = orc.adamw_scalars(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)
+    for _ in range(rep):
+        for (_, p, m, v), mean in zip(host, means):
+            orc.adamw_update(mean, d.clip_coef, s, p, m, v)
+    el = time.perf_counter() - t0
+    step_s = el * E / n_s
+    traffic = (Rk * 4 + 4) * E + (4 + 24 * rep) * E
+    return {"value_ms_per_step": round(step_s * 1e3, 1),
+            "traffic_gbs": round(traffic / step_s / 1e9, 4), "cores": 1, "kind": "oracle",
+            "host": host_info(),
+            "sample": "first %d tensors (%d elements, %.2f s single-threaded), scaled by "
+                      "element count to the %d-element step" % (len(host), n_s, el, E)}
 
 
 def bench_case(args):
@@ -579,7 +685,8 @@ def bench_case(args):
         sets = rcc.ParamSets([dict(grads=ins, params=[p0], exp_avg=[torch.zeros_like(p0)],
                                    exp_avg_sq=[torch.zeros_like(p0)],
                                    mean_grad=torch.empty_like(p0))])
-        cfg, state = rcc.adamw_cfg(replicas=1), rcc.optim_state(scale=1.0)
+        cfg = rcc.adamw_cfg(replicas=1, flags=gs_flags(rcc, args.gs_mode))
+        state = rcc.optim_state(scale=1.0)
         traffic = (Rk * 4 + 4) * n + 28 * n
 
     def once():
@@ -616,6 +723,7 @@ def bench_case(args):
     med = statistics.median(ms)
     print(json.dumps({"case": c, "ranks": Rk, "elems": n, "dtype": args.dtype, "op": args.op,
                       "mode": "fast" if args.fast else "deterministic",
+                      **({"gs_mode": args.gs_mode} if c == "grad_sync" else {}),
                       "median_ms": round(med, 5), "min_ms": round(min(ms), 5),
                       "algbw_gbs": round(Rk * n * es / (med * 1e-3) / 1e9, 1),
                       "traffic_gbs": round(traffic / (med * 1e-3) / 1e9, 1),

@@ -216,9 +216,11 @@ __global__ void __launch_bounds__(kThreads)
   block_reduce_row(s, c, out + (uint64_t)blockIdx.x * 3);
 }
 
-// the final reduction into the 12-byte report (one block, any row count)
+// the final reduction into the 12-byte report (one block, any row count);
+// thread 0, which wrote the report, also stores it to the host's mapped slot
 __global__ void __launch_bounds__(kThreads)
-    gs_report_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ report) {
+    gs_report_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ report,
+                     uint32_t* __restrict__ host_copy) {
   double s = 0.0;
   uint32_t c = 0;
   for (uint64_t r = threadIdx.x; r < nrows; r += kThreads) {
@@ -226,6 +228,11 @@ __global__ void __launch_bounds__(kThreads)
     c += in[r * 3 + 2];
   }
   block_reduce_row(s, c, report);
+  if (host_copy && threadIdx.x == 0) {
+    host_copy[0] = report[0];
+    host_copy[1] = report[1];
+    host_copy[2] = report[2];
+  }
 }
 
 // ---- AdamW update ---------------------------------------------------------
@@ -467,8 +474,8 @@ cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
 }
 
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
-                             cudaStream_t stream) {
-  gs::gs_report_kernel<<<1, kThreads, 0, stream>>>(in, nrows, report);
+                             uint32_t* host_copy, cudaStream_t stream) {
+  gs::gs_report_kernel<<<1, kThreads, 0, stream>>>(in, nrows, report, host_copy);
   return cudaGetLastError();
 }
 
@@ -684,7 +691,7 @@ extern "C" rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_
     n = (n + gs::kFanIn - 1) / gs::kFanIn;
     ++launched;
   }
-  if ((e = launch_gs_report(src, n, report, cs)) != cudaSuccess)
+  if ((e = launch_gs_report(src, n, report, nullptr, cs)) != cudaSuccess)
     return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
   add_launches(launched + 1);
   return RCC_OK;

@@ -90,7 +90,9 @@ struct Scratch {
   size_t rows_cap = 0;
   void* combine = nullptr;          // the reused reduction region, kCombineRegionBytes
   uint32_t* report_dev = nullptr;   // 12-byte report (16 allocated)
-  uint32_t* report_host = nullptr;  // pinned readback slot
+  uint32_t* report_host = nullptr;  // pinned, mapped readback slot
+  uint32_t* report_host_dev = nullptr;  // its device alias (the report kernel writes it), or
+                                        // null: then a 12-byte D2H copy fills the slot
   void* desc_dev = nullptr;         // tensor table + grad table + state table
   size_t desc_cap = 0;
   void* desc_host = nullptr;        // pinned staging for the tables

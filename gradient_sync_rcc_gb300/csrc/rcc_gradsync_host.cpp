@@ -33,8 +33,15 @@ rcc_status ensure_fixed_scratch(Scratch& sc) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(report)");
   }
   if (!sc.report_host) {
-    e = cudaMallocHost(reinterpret_cast<void**>(&sc.report_host), 16);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(report)");
+    e = cudaHostAlloc(reinterpret_cast<void**>(&sc.report_host), 16, cudaHostAllocMapped);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(report)");
+    // the report kernel stores the 12 bytes straight into this slot, so no
+    // copy is queued between the report and the host's wait
+    void* alias = nullptr;
+    if (cudaHostGetDevicePointer(&alias, sc.report_host, 0) == cudaSuccess)
+      sc.report_host_dev = static_cast<uint32_t*>(alias);
+    else
+      (void)cudaGetLastError();
   }
   if (!sc.report_ev) {
     e = cudaEventCreateWithFlags(&sc.report_ev, cudaEventDisableTiming);
@@ -302,11 +309,13 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       ++levels;
     }
   }
-  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, cs)) != cudaSuccess)
+  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, cs)) !=
+      cudaSuccess)
     return cuda_fail(e, "report kernel");
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  if ((e = cudaMemcpyAsync(sc.report_host, sc.report_dev, 12, cudaMemcpyDeviceToHost, cs)) !=
-      cudaSuccess)
+  if (!sc.report_host_dev &&
+      (e = cudaMemcpyAsync(sc.report_host, sc.report_dev, 12, cudaMemcpyDeviceToHost, cs)) !=
+          cudaSuccess)
     return cuda_fail(e, "report readback");
   if ((e = cudaEventRecord(sc.report_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
 
@@ -329,6 +338,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   };
   auto enqueue_branched = [&](cudaStream_t origin) -> cudaError_t {
     cudaError_t le;
+    const int nb = (int)std::min<size_t>(P, Scratch::kBranches);
+    if (nb == 1) return enqueue_one(0, origin);  // one tensor: no fork/join
     if (!sc.fork_ev && (le = cudaEventCreateWithFlags(&sc.fork_ev, cudaEventDisableTiming)))
       return le;
     for (int k = 0; k < Scratch::kBranches; ++k) {
@@ -340,21 +351,21 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
         return le;
     }
     if ((le = cudaEventRecord(sc.fork_ev, origin)) != cudaSuccess) return le;
-    for (int k = 0; k < Scratch::kBranches; ++k)
+    for (int k = 0; k < nb; ++k)
       if ((le = cudaStreamWaitEvent(sc.branch[k], sc.fork_ev, 0)) != cudaSuccess) return le;
     std::vector<size_t> order(P);
     for (size_t p = 0; p < P; ++p) order[p] = p;
     std::stable_sort(order.begin(), order.end(),
                      [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
-    uint64_t load[Scratch::kBranches] = {};
+    uint64_t load[Scratch::kBranches] = {};  // chains used: nb = min(P, 8)
     for (size_t p : order) {
       int k = 0;
-      for (int j = 1; j < Scratch::kBranches; ++j)
+      for (int j = 1; j < nb; ++j)
         if (load[j] < load[k]) k = j;
       load[k] += params[p].numel;
       if ((le = enqueue_one(p, sc.branch[k])) != cudaSuccess) return le;
     }
-    for (int k = 0; k < Scratch::kBranches; ++k) {
+    for (int k = 0; k < nb; ++k) {
       if ((le = cudaEventRecord(sc.join_ev[k], sc.branch[k])) != cudaSuccess) return le;
       if ((le = cudaStreamWaitEvent(origin, sc.join_ev[k], 0)) != cudaSuccess) return le;
     }
