@@ -79,7 +79,7 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="size sweep: all_reduce mean (fp32, bf16), broadcast root 0 and reduce "
                          "root R-1 for R in {2,4,8}, N = 257*4^k and 2^28; one JSON line per point")
-    ap.add_argument("--gs-mode", default="host", choices=["host", "device", "graph", "multi"],
+    ap.add_argument("--gs-mode", default="host", choices=["host", "device", "graph", "multi", "host_graph"],
                     help="grad-sync decision: host readback (default), device kernel, or device "
                          "kernel + captured update launches")
     return ap.parse_args()
@@ -560,7 +560,8 @@ def bench_reference(args):
 def gs_flags(rcc, mode):
     """`--gs-mode` -> rcc_adamw_cfg.flags."""
     return {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
-            "multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR}[mode]
+            "multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR,
+            "host_graph": rcc.ADAMW_HOST_GRAPH}[mode]
 
 
 def bench_grad_sync_1024(args):

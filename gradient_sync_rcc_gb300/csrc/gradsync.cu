@@ -114,11 +114,19 @@ __device__ __forceinline__ void block_reduce_row(double s, uint32_t c, uint32_t*
   }
 }
 
+// s / R rounded once.  For R a power of two the product s * (1/R) is the
+// same correctly rounded quotient -- scaling by 2^-k rounds the same real
+// number once, subnormal results included -- at a fraction of a division's
+// instructions; other R divide.
+__device__ __forceinline__ float div_by_ranks(float s, int R) {
+  return (R & (R - 1)) == 0 ? __fmul_rn(s, __frcp_rn((float)R)) : __fdiv_rn(s, (float)R);
+}
+
 // mean of R scaled gradients in rank order, then unscale: both steps fp32 IEEE
 __device__ __forceinline__ float mean_unscale(const float* x, int R, float inv_scale) {
   float s = x[0];
   for (int q = 1; q < R; ++q) s = __fadd_rn(s, x[q]);
-  return __fmul_rn(__fdiv_rn(s, (float)R), inv_scale);
+  return __fmul_rn(div_by_ranks(s, R), inv_scale);
 }
 
 template <int RC>  // RC > 0: compile-time rank count; 0: runtime (a.R)
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constan
           } else {
             float s = g[0][vi * 4 + e];
             for (int q = 1; q < R; ++q) s = __fadd_rn(s, g[q][vi * 4 + e]);
-            m[e] = __fmul_rn(__fdiv_rn(s, (float)R), a.inv_scale);
+            m[e] = __fmul_rn(div_by_ranks(s, R), a.inv_scale);
           }
           acc.add(m[e]);
         }
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constan
   for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads) {
     float s = g[0][i];
     for (int q = 1; q < R; ++q) s = __fadd_rn(s, g[q][i]);
-    const float m = __fmul_rn(__fdiv_rn(s, (float)R), a.inv_scale);
+    const float m = __fmul_rn(div_by_ranks(s, R), a.inv_scale);
     acc.add(m);
     if (t.mean_grad) t.mean_grad[i] = m;
   }
@@ -317,9 +325,8 @@ __device__ __forceinline__ bool update_vec4(float* const* P, int rep, const floa
   if (sv.d.skip) return false;  // skipped step: state untouched
   float gv[4] = {g4.x, g4.y, g4.z, g4.w};
   if (!mean_grad) {
-    const float Rf = (float)R;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(__fdiv_rn(gv[e], Rf), sv.inv_scale);
+    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(div_by_ranks(gv[e], R), sv.inv_scale);
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], sv.d.coef);
@@ -361,7 +368,7 @@ __device__ __forceinline__ void update_one(float* const* P, int rep, const float
   } else {
     float s = grads[0][i];
     for (int q = 1; q < R; ++q) s = __fadd_rn(s, grads[q][i]);
-    g = __fmul_rn(__fdiv_rn(s, (float)R), sv.inv_scale);
+    g = __fmul_rn(div_by_ranks(s, R), sv.inv_scale);
   }
   g = __fmul_rn(g, sv.d.coef);
   for (int r = 0; r < rep; ++r) {

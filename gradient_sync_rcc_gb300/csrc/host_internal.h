@@ -106,6 +106,7 @@ struct Scratch {
   rcc::GsDecision* decision_dev = nullptr;
   rcc::AdamWScalars* scalars_dev = nullptr;
   rcc::AdamWScalars* scalars_host = nullptr;  // pinned staging
+  rcc::GsDecision* decision_host = nullptr;   // pinned staging of a host decision
   // captured update launches: a fork/join graph of kBranches parallel chains
   static constexpr int kBranches = 8;
   cudaStream_t capture_stream = nullptr;
@@ -185,6 +186,7 @@ inline void free_scratch(Scratch& s) {
   if (s.decision_dev) cudaFree(s.decision_dev);
   if (s.scalars_dev) cudaFree(s.scalars_dev);
   if (s.scalars_host) cudaFreeHost(s.scalars_host);
+  if (s.decision_host) cudaFreeHost(s.decision_host);
   if (s.graph_exec) cudaGraphExecDestroy(s.graph_exec);
   if (s.capture_stream) cudaStreamDestroy(s.capture_stream);
   for (int k = 0; k < Scratch::kBranches; ++k) {

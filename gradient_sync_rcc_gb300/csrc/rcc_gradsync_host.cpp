@@ -68,6 +68,10 @@ rcc_status ensure_decision_scratch(Scratch& sc) {
     e = cudaMallocHost(reinterpret_cast<void**>(&sc.scalars_host), sizeof(rcc::AdamWScalars));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(scalars)");
   }
+  if (!sc.decision_host) {
+    e = cudaMallocHost(reinterpret_cast<void**>(&sc.decision_host), sizeof(rcc::GsDecision));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(decision)");
+  }
   return RCC_OK;
 }
 
@@ -133,8 +137,12 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return fail(RCC_ERR_INVALID_ARGUMENT, "gradient sync needs an RCC_F32 session");
   if (rep != 1 && rep != R)
     return fail(RCC_ERR_INVALID_ARGUMENT, "replicas %d must be 1 or %d", rep, R);
-  if (cfg->flags & ~(RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH | RCC_ADAMW_MULTI_TENSOR))
+  if (cfg->flags & ~(RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH | RCC_ADAMW_MULTI_TENSOR |
+                     RCC_ADAMW_HOST_GRAPH))
     return fail(RCC_ERR_INVALID_ARGUMENT, "unknown cfg->flags bits 0x%x", cfg->flags);
+  if ((cfg->flags & RCC_ADAMW_HOST_GRAPH) && (cfg->flags & ~RCC_ADAMW_HOST_GRAPH))
+    return fail(RCC_ERR_INVALID_ARGUMENT, "RCC_ADAMW_HOST_GRAPH takes no other flag (it is the "
+                                          "host decision with the captured update launches)");
   if ((cfg->flags & RCC_ADAMW_GRAPH) && (cfg->flags & RCC_ADAMW_MULTI_TENSOR))
     return fail(RCC_ERR_INVALID_ARGUMENT, "RCC_ADAMW_GRAPH and RCC_ADAMW_MULTI_TENSOR exclude "
                                           "each other (the multi-tensor update is one launch)");
@@ -264,9 +272,11 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     ++sc.desc_gen;
   }
   const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
+  const bool host_graph = (cfg->flags & RCC_ADAMW_HOST_GRAPH) != 0;
   const int64_t t_next = state->step + 1;
-  if (on_device) {
-    // the scalars of step t+1; used only if the device decides not to skip
+  if (on_device || host_graph) {
+    // the scalars of step t+1, read by the updates from device memory; used
+    // only if the step is not skipped
     if ((st = ensure_decision_scratch(sc)) != RCC_OK) return st;
     *sc.scalars_host = step_scalars(cfg, t_next);
     sc.scalars_host->inv_scale = (float)(1.0 / state->scale);
@@ -353,18 +363,42 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     if ((le = cudaEventRecord(sc.fork_ev, origin)) != cudaSuccess) return le;
     for (int k = 0; k < nb; ++k)
       if ((le = cudaStreamWaitEvent(sc.branch[k], sc.fork_ev, 0)) != cudaSuccess) return le;
+    // Chains: tensors taken largest first, each onto the least loaded chain,
+    // a launch counting as kLaunchCost elements of fixed cost.  Each chain
+    // then runs its tensors alternately from its largest and its smallest
+    // end, so the small, latency-bound launches of one chain overlap large,
+    // bandwidth-bound ones on the others instead of every chain ending on a
+    // run of small ones.  Launches are issued round-robin over the chains.
+    constexpr uint64_t kLaunchCost = 65536;
     std::vector<size_t> order(P);
     for (size_t p = 0; p < P; ++p) order[p] = p;
     std::stable_sort(order.begin(), order.end(),
                      [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
-    uint64_t load[Scratch::kBranches] = {};  // chains used: nb = min(P, 8)
+    std::vector<size_t> chain[Scratch::kBranches];
+    uint64_t load[Scratch::kBranches] = {};
     for (size_t p : order) {
       int k = 0;
       for (int j = 1; j < nb; ++j)
         if (load[j] < load[k]) k = j;
-      load[k] += params[p].numel;
-      if ((le = enqueue_one(p, sc.branch[k])) != cudaSuccess) return le;
+      load[k] += params[p].numel + kLaunchCost;
+      chain[k].push_back(p);
     }
+    size_t longest = 0;
+    for (int k = 0; k < nb; ++k) {
+      std::vector<size_t>& c = chain[k];
+      std::vector<size_t> alt;
+      alt.reserve(c.size());
+      for (size_t lo = 0, hi = c.size(); lo < hi;) {
+        alt.push_back(c[lo++]);
+        if (lo < hi) alt.push_back(c[--hi]);
+      }
+      c.swap(alt);
+      longest = std::max(longest, c.size());
+    }
+    for (size_t pos = 0; pos < longest; ++pos)
+      for (int k = 0; k < nb; ++k)
+        if (pos < chain[k].size() && (le = enqueue_one(chain[k][pos], sc.branch[k])) != cudaSuccess)
+          return le;
     for (int k = 0; k < nb; ++k) {
       if ((le = cudaEventRecord(sc.join_ev[k], sc.branch[k])) != cudaSuccess) return le;
       if ((le = cudaStreamWaitEvent(origin, sc.join_ev[k], 0)) != cudaSuccess) return le;
@@ -391,6 +425,41 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return rcc::launch_gs_update_multi(ma, where);
   };
   const uint64_t launches_per_update = multi ? 1 : P;
+  // The per-tensor updates captured once into a graph that reads the
+  // decision and the scalars from device memory, replayed while the tables
+  // stay the same.
+  auto replay_graph = [&]() -> rcc_status {
+    ua.clip_coef = 1.0f;
+    ua.decision = sc.decision_dev;
+    ua.dev_scalars = sc.scalars_dev;
+    if (!sc.graph_exec || sc.graph_gen != sc.desc_gen || sc.graph_P != P) {
+      // capture the P update launches once for these tables
+      if (sc.graph_exec) cudaGraphExecDestroy(sc.graph_exec);
+      sc.graph_exec = nullptr;
+      if (!sc.capture_stream &&
+          (e = cudaStreamCreateWithFlags(&sc.capture_stream, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "cudaStreamCreate");
+      if ((e = cudaStreamBeginCapture(sc.capture_stream, cudaStreamCaptureModeThreadLocal)) !=
+          cudaSuccess)
+        return cuda_fail(e, "cudaStreamBeginCapture");
+      cudaError_t le = enqueue_branched(sc.capture_stream);
+      cudaGraph_t graph = nullptr;
+      e = cudaStreamEndCapture(sc.capture_stream, &graph);
+      if (le != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return cuda_fail(le, "update capture");
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+      e = cudaGraphInstantiate(&sc.graph_exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+      sc.graph_gen = sc.desc_gen;
+      sc.graph_P = P;
+    }
+    if ((e = cudaGraphLaunch(sc.graph_exec, cs)) != cudaSuccess)
+      return cuda_fail(e, "cudaGraphLaunch");
+    return RCC_OK;
+  };
 
   uint64_t device_updates = 0;
   if (on_device) {
@@ -403,32 +472,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     ua.decision = sc.decision_dev;
     ua.dev_scalars = sc.scalars_dev;
     if (cfg->flags & RCC_ADAMW_GRAPH) {
-      if (!sc.graph_exec || sc.graph_gen != sc.desc_gen || sc.graph_P != P) {
-        // capture the P update launches once for these tables
-        if (sc.graph_exec) cudaGraphExecDestroy(sc.graph_exec);
-        sc.graph_exec = nullptr;
-        if (!sc.capture_stream &&
-            (e = cudaStreamCreateWithFlags(&sc.capture_stream, cudaStreamNonBlocking)) != cudaSuccess)
-          return cuda_fail(e, "cudaStreamCreate");
-        if ((e = cudaStreamBeginCapture(sc.capture_stream, cudaStreamCaptureModeThreadLocal)) !=
-            cudaSuccess)
-          return cuda_fail(e, "cudaStreamBeginCapture");
-        cudaError_t le = enqueue_branched(sc.capture_stream);
-        cudaGraph_t graph = nullptr;
-        e = cudaStreamEndCapture(sc.capture_stream, &graph);
-        if (le != cudaSuccess) {
-          if (graph) cudaGraphDestroy(graph);
-          return cuda_fail(le, "update capture");
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
-        e = cudaGraphInstantiate(&sc.graph_exec, graph, 0);
-        cudaGraphDestroy(graph);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
-        sc.graph_gen = sc.desc_gen;
-        sc.graph_P = P;
-      }
-      if ((e = cudaGraphLaunch(sc.graph_exec, cs)) != cudaSuccess)
-        return cuda_fail(e, "cudaGraphLaunch");
+      if ((st = replay_graph()) != RCC_OK) return st;
     } else {
       if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess)
         return cuda_fail(e, "update kernel");
@@ -473,10 +517,20 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     }
   } else {
     const int64_t t = t_next;
-    ua.s = step_scalars(cfg, t);
-    ua.clip_coef = coef;
-    if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess)
-      return cuda_fail(e, "update kernel");
+    if (host_graph) {
+      // the host's decision goes to device memory for the replayed graph
+      sc.decision_host->skip = 0u;
+      sc.decision_host->coef = coef;
+      if ((e = cudaMemcpyAsync(sc.decision_dev, sc.decision_host, sizeof(rcc::GsDecision),
+                               cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+        return cuda_fail(e, "decision upload");
+      if ((st = replay_graph()) != RCC_OK) return st;
+    } else {
+      ua.s = step_scalars(cfg, t);
+      ua.clip_coef = coef;
+      if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess)
+        return cuda_fail(e, "update kernel");
+    }
     g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
     rep_out.update_launches = launches_per_update;
     state->step = t;

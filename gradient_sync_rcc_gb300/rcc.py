@@ -35,6 +35,7 @@ DETERMINISTIC = 0x1
 ADAMW_DEVICE_DECISION = 0x1
 ADAMW_GRAPH = 0x2
 ADAMW_MULTI_TENSOR = 0x4
+ADAMW_HOST_GRAPH = 0x8
 MAX_RANKS = 64
 
 # every symbol include/rcc.h declares

@@ -248,10 +248,16 @@ typedef struct {
  *   and sizes stay the same (still one kernel node per parameter tensor).
  * RCC_ADAMW_MULTI_TENSOR: one update launch covers every tensor (one CTA per
  *   statistics row) instead of one launch per tensor -- a comparison point
- *   against the pages' one-kernel-per-parameter design; not with GRAPH. */
+ *   against the pages' one-kernel-per-parameter design; not with GRAPH.
+ * RCC_ADAMW_HOST_GRAPH: the pages' order (report read back, decision on the
+ *   host), then one 8-byte copy puts the decision in device memory and the
+ *   captured per-tensor update graph of RCC_ADAMW_GRAPH is replayed instead of
+ *   P separate launches; a skipped step launches nothing.  Takes no other
+ *   flag. */
 #define RCC_ADAMW_DEVICE_DECISION 0x1u
 #define RCC_ADAMW_GRAPH 0x2u
 #define RCC_ADAMW_MULTI_TENSOR 0x4u
+#define RCC_ADAMW_HOST_GRAPH 0x8u
 
 /* Optimizer step count and GradScaler state, owned by the caller, updated by
  * each call ([RUDA-T]: scale -> step -> update on the same GradScaler). */

@@ -120,7 +120,8 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
 
 MODES = {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
          "multi": rcc.ADAMW_MULTI_TENSOR,
-         "device_multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR}
+         "device_multi": rcc.ADAMW_DEVICE_DECISION | rcc.ADAMW_MULTI_TENSOR,
+         "host_graph": rcc.ADAMW_HOST_GRAPH}
 
 
 @pytest.mark.parametrize("mode", list(MODES))
@@ -155,34 +156,43 @@ def test_decision_modes_bitwise_identical():
         assert state.step == 5
         finals[mode] = [torch.cat([t["params"][1], t["exp_avg"][0], t["exp_avg_sq"][1]]).cpu()
                         for t in prob.tensors]
-    for mode in ("device", "graph", "multi", "device_multi"):
+    for mode in (m for m in MODES if m != "host"):
         for a, b in zip(finals["host"], finals[mode]):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32)), mode
 
 
-def test_graph_recaptured_when_tensors_change(orc):
+@pytest.mark.parametrize("flags", [rcc.ADAMW_GRAPH, rcc.ADAMW_HOST_GRAPH])
+def test_graph_recaptured_when_tensors_change(orc, flags):
     """New gradient buffers change the descriptor tables; the graph must follow."""
     sizes = [10000, 2000, 777]
     prob = Problem(2, sizes, 32, 1, True)
-    run_steps(orc, prob, 2, None, {"flags": rcc.ADAMW_GRAPH})
+    run_steps(orc, prob, 2, None, {"flags": flags})
     for t in prob.tensors:
         t["grads"] = [torch.empty_like(g) for g in t["grads"]]
         t["mean_grad"] = torch.empty_like(t["mean_grad"])
     prob.sets = rcc.ParamSets(prob.tensors)
-    run_steps(orc, prob, 2, None, {"flags": rcc.ADAMW_GRAPH})
+    run_steps(orc, prob, 2, None, {"flags": flags})
 
 
-def test_mean_grad_output_bitwise(orc):
-    R = 4
+@pytest.mark.parametrize("R", [3, 4, 5, 8])
+@pytest.mark.parametrize("scale", [65536.0, 1.0])
+def test_mean_grad_output_bitwise(orc, R, scale):
+    """The stored mean gradient, bit for bit: the division by R (a multiply by
+    the exact reciprocal when R is a power of two) and the unscale.  At scale 1
+    the subnormal sums below reach the output, so the rounding of s / R at the
+    bottom of the range is checked too."""
     sizes = [1, 3, 4099, 70001]
     prob = Problem(R, sizes, 12, 1, True)
-    grads = prob.host_grads(1, 65536.0)
+    grads = prob.host_grads(1, scale)
+    tiny = np.array([1, 3, 7, 5, -9, 2, 11, 6], np.float32) * np.float32(2.0 ** -149)
+    for r in range(R):
+        grads[3][r][:8] = tiny * np.float32(r + 1)
     prob.load_grads(grads)
     cfg = rcc.adamw_cfg(replicas=1)
     with session(R) as h:
-        rcc.grad_sync_adamw(h, prob.sets, cfg, rcc.optim_state())
+        rcc.grad_sync_adamw(h, prob.sets, cfg, rcc.optim_state(scale=scale))
         torch.cuda.synchronize()
-    inv = np.float32(1.0 / 65536.0)
+    inv = np.float32(1.0 / scale)
     for i in range(len(sizes)):
         want = orc.mean_unscale(grads[i], inv)
         assert bits_equal(to_host(prob.tensors[i]["mean_grad"]), want)
@@ -344,3 +354,13 @@ def test_overlapping_outputs_rejected_shared_grads_allowed():
         rep = rcc.grad_sync_adamw(h, rcc.ParamSets([t1, fine]), cfg, rcc.optim_state(scale=1.0))
         torch.cuda.synchronize()
     assert rep.update_launches == 2
+
+
+@pytest.mark.parametrize("R", [3, 6])
+@pytest.mark.parametrize("mean_grad", [True, False])
+def test_rank_counts_that_are_not_powers_of_two(orc, R, mean_grad):
+    """R = 3 and 6 divide (no exact reciprocal); with no stored mean gradient
+    the update recomputes the mean with the same arithmetic."""
+    sizes = [5000, 1023, 64]
+    prob = Problem(R, sizes, 17, 1, mean_grad)
+    run_steps(orc, prob, 3, None, {})
