@@ -76,6 +76,8 @@ def parse_args():
     ap.add_argument("--op", default="sum", choices=["sum", "mean", "max", "min"])
     ap.add_argument("--fast", action="store_true", help="pairwise-tree sums instead of rank order")
     ap.add_argument("--replicas", type=int, default=1, help="optimizer-state copies (grad_sync_1024)")
+    ap.add_argument("--elems-per-row", type=int, default=0,
+                    help="statistics row size for the grad-sync cases (0: the library default)")
     ap.add_argument("--sweep", action="store_true",
                     help="size sweep: all_reduce mean (fp32, bf16), broadcast root 0 and reduce "
                          "root R-1 for R in {2,4,8}, N = 257*4^k and 2^28; one JSON line per point")
@@ -585,7 +587,8 @@ def bench_grad_sync_1024(args):
                             exp_avg_sq=[torch.zeros(n, device=dev) for _ in range(rep)],
                             mean_grad=torch.empty(n, device=dev)))
     sets = rcc.ParamSets(tensors)
-    cfg = rcc.adamw_cfg(replicas=rep, flags=gs_flags(rcc, args.gs_mode))
+    cfg = rcc.adamw_cfg(replicas=rep, flags=gs_flags(rcc, args.gs_mode),
+                        elems_per_row=args.elems_per_row)
     state = rcc.optim_state(scale=65536.0)
     h = rcc.register(0, Rk, rcc.F32, True)
     try:
@@ -686,7 +689,8 @@ def bench_case(args):
         sets = rcc.ParamSets([dict(grads=ins, params=[p0], exp_avg=[torch.zeros_like(p0)],
                                    exp_avg_sq=[torch.zeros_like(p0)],
                                    mean_grad=torch.empty_like(p0))])
-        cfg = rcc.adamw_cfg(replicas=1, flags=gs_flags(rcc, args.gs_mode))
+        cfg = rcc.adamw_cfg(replicas=1, flags=gs_flags(rcc, args.gs_mode),
+                            elems_per_row=args.elems_per_row)
         state = rcc.optim_state(scale=1.0)
         traffic = (Rk * 4 + 4) * n + 28 * n
 

@@ -54,6 +54,38 @@ __device__ __forceinline__ void st_vec(void* p, const uint4& v) {
                : "memory");
 }
 
+// 32-byte global accesses (sm_100 and later): one request per warp for 1 KiB.
+struct Words8 {
+  uint32_t w[8];
+};
+
+// An L2 policy that marks lines evict-first: for the gradients, read once,
+// so that the mean gradient written beside them is what L2 keeps.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ Words8 ld_vec8(const void* p, uint64_t l2_policy) {
+  Words8 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+        "=r"(v.w[6]), "=r"(v.w[7])
+      : "l"(p), "l"(l2_policy));
+  return v;
+}
+
+// Write-back store: the mean gradient is read again by the update kernels
+// right after, so it is left to stay in L2 as long as it can.
+__device__ __forceinline__ void st_vec8(void* p, const Words8& v) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
+               : "memory");
+}
+
 // ---- per-thread sum of squares -------------------------------------------
 // The squares are summed in a pair of fp32 words (value + running error) with
 // error-free transformations: the product error fmaf(g, g, -g*g) is exact and
@@ -129,8 +161,10 @@ __device__ __forceinline__ float mean_unscale(const float* x, int R, float inv_s
   return __fmul_rn(div_by_ranks(s, R), inv_scale);
 }
 
+// Register budget: 3 CTAs per SM at eight ranks (8 x 32-byte vectors in
+// flight per thread), 4 below that.
 template <int RC>  // RC > 0: compile-time rank count; 0: runtime (a.R)
-__global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constant__ GsStatsArgs a) {
+__global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(const __grid_constant__ GsStatsArgs a) {
   const uint64_t row = blockIdx.x;
   // the tensor owning this row: last t with row_begin <= row
   uint32_t lo = 0, hi = a.num_tensors - 1;
@@ -150,15 +184,43 @@ __global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constan
 
   SqAcc acc;
   uint64_t scalar_from = c0;
-  if (t.vec_ok & 1u) {
-    // c0 is a multiple of 4 (elems_per_row is), so vectors start aligned
+  if constexpr (RC > 0) {
+    if (t.vec_ok & 4u) {
+      // 32-byte vectors: the host sets bit 2 only when every gradient (and
+      // the mean gradient) is 32-byte aligned and elems_per_row is a
+      // multiple of 8, so c0 starts a vector
+      const uint64_t v0 = c0 / 8, v1 = c1 / 8;
+      scalar_from = v1 * 8;
+      const uint64_t pol = l2_evict_first_policy();
+      for (uint64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
+        Words8 x[RC];
+#pragma unroll
+        for (int q = 0; q < RC; ++q) x[q] = ld_vec8(g[q] + v * 8, pol);
+        Words8 m;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float col[RC];
+#pragma unroll
+          for (int q = 0; q < RC; ++q) col[q] = __uint_as_float(x[q].w[e]);
+          const float me = mean_unscale(col, RC, a.inv_scale);
+          acc.add(me);
+          m.w[e] = __float_as_uint(me);
+        }
+        if (t.mean_grad) st_vec8(t.mean_grad + v * 8, m);
+      }
+    }
+  }
+  if (scalar_from == c0 && (t.vec_ok & 1u)) {
+    // c0 is a multiple of 4 (elems_per_row is), so vectors start aligned;
+    // two vectors per rank in flight, one at eight ranks (register budget)
+    constexpr int kU4 = RC >= 8 ? 1 : 2;
     const uint64_t v0 = c0 / 4, v1 = c1 / 4;
     scalar_from = v1 * 4;
-    for (uint64_t v = v0 + threadIdx.x; v < v1; v += 2 * kThreads) {
-      uint4 x[2][RC > 0 ? RC : 1];
+    for (uint64_t v = v0 + threadIdx.x; v < v1; v += kU4 * kThreads) {
+      uint4 x[kU4][RC > 0 ? RC : 1];
       if constexpr (RC > 0) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kU4; ++u) {
           const uint64_t vi = v + (uint64_t)u * kThreads;
           if (vi < v1) {
 #pragma unroll
@@ -167,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) gs_stats_kernel(const __grid_constan
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kU4; ++u) {
         const uint64_t vi = v + (uint64_t)u * kThreads;
         if (vi >= v1) continue;
         float m[4];

@@ -250,6 +250,7 @@ inline bool overlap(const void* a, size_t an, const void* b, size_t bn) {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // Byte ranges that must not overlap one another; returns the indices of an
 // overlapping pair, or {-1, -1}.  Sorting keeps this O(n log n) for the R*R

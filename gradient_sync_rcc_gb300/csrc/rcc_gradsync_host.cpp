@@ -209,13 +209,22 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   auto* gtab = reinterpret_cast<const float**>(desc.data() + off_grads);
   auto* stab = reinterpret_cast<float**>(desc.data() + off_state);
   std::vector<int> upd_vec(P);
+  // 32-byte statistics vectors need rows that start on 8 elements
+  // (RCC_VEC_BYTES=16 caps every kernel at 16-byte vectors)
+  static const bool wide_ok = [] {
+    const char* v = std::getenv("RCC_VEC_BYTES");
+    return !(v && std::atoi(v) == 16);
+  }();
+  const bool rows8 = wide_ok && epr % 8 == 0;
   uint64_t row = 0;
   for (size_t p = 0; p < P; ++p) {
     const rcc_param_set& ps = params[p];
     bool gv = ps.mean_grad == nullptr || aligned16(ps.mean_grad);
+    bool gv32 = rows8 && (ps.mean_grad == nullptr || aligned32(ps.mean_grad));
     for (int r = 0; r < R; ++r) {
       gtab[p * R + r] = ps.grads[r];
       gv = gv && aligned16(ps.grads[r]);
+      gv32 = gv32 && aligned32(ps.grads[r]);
     }
     bool uv = gv;
     for (int k = 0; k < rep; ++k) {
@@ -230,7 +239,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     t.row_begin = row;
     t.mean_grad = ps.mean_grad;
     t.grad_slot = (uint32_t)(p * R);
-    t.vec_ok = (gv ? 1u : 0u) | (uv ? 2u : 0u);
+    t.vec_ok = (gv ? 1u : 0u) | (uv ? 2u : 0u) | (gv32 ? 4u : 0u);
     tens[p] = t;
     row += (ps.numel + epr - 1) / epr;
   }

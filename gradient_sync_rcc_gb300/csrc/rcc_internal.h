@@ -65,7 +65,9 @@ struct GsTensor {
   float* mean_grad;         // optional output of the unscaled mean gradient
   uint32_t grad_slot;       // index of this tensor's R grad pointers in the grad table
   uint32_t vec_ok;          // bit 0: all R grads (and mean_grad) 16-byte aligned;
-                            // bit 1: so are all its state pointers (update vectors)
+                            // bit 1: so are all its state pointers (update vectors);
+                            // bit 2: grads and mean_grad 32-byte aligned and rows
+                            //        a multiple of 8 elements (32-byte statistics)
 };
 
 struct GsStatsArgs {
