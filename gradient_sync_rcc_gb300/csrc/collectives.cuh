@@ -22,6 +22,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "launch.cuh"
 #include "rcc_internal.h"
 
 namespace rcc {
@@ -283,6 +284,7 @@ struct SegView {
 // the host picks 8 only when every address is 32-byte aligned.
 template <typename T, int NS, int RED, bool FAST, int U, int W>
 __global__ void RCC_BOUNDS mp_kernel(const __grid_constant__ MultiPtrArgs a) {
+  pdl_wait_then_release();
   using E = Elem<T>;
   constexpr int EPV = W * E::kPerWord;  // elements per vector
   constexpr int VB = 4 * W;             // bytes per vector
@@ -491,6 +493,7 @@ template <int EB>
 __global__ void __launch_bounds__(32) bulk_copy_kernel(const __grid_constant__ MultiPtrArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[kBulkStages];
+  pdl_wait_then_release();
   if (threadIdx.x != 0) return;
   const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
                    (size_t)blockIdx.y * a.dst_seg_stride};
@@ -585,8 +588,7 @@ cudaError_t launch_bulk_copy(int nseg, const MultiPtrArgs& a, cudaStream_t strea
   size_t cap = (size_t)per_sm * sm_count() / (size_t)nseg;
   if (cap < 1) cap = 1;
   const unsigned gx = (unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap);
-  bulk_copy_kernel<EB><<<dim3(gx, (unsigned)nseg), 32, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(bulk_copy_kernel<EB>, dim3(gx, (unsigned)nseg), dim3(32), smem, stream, a);
 }
 
 // Reads and clears this translation unit's bulk-copy timeout flag.
@@ -622,8 +624,7 @@ cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   size_t cap = (size_t)resident_blocks((const void*)fn) * sm_count() * RCC_WAVES / (size_t)nseg;
   if (cap < 1) cap = 1;
   const unsigned gx = (unsigned)(want < cap ? want : cap);
-  fn<<<dim3(gx, (unsigned)nseg), kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(fn, dim3(gx, (unsigned)nseg), dim3(kThreads), 0, stream, a);
 }
 
 template <typename T, int NS, int RED, bool FAST>

@@ -26,6 +26,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "launch.cuh"
 #include "rcc.h"
 #include "rcc_internal.h"
 
@@ -165,6 +166,7 @@ __device__ __forceinline__ float mean_unscale(const float* x, int R, float inv_s
 // flight per thread), 4 below that.
 template <int RC>  // RC > 0: compile-time rank count; 0: runtime (a.R)
 __global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(const __grid_constant__ GsStatsArgs a) {
+  pdl_wait_then_release();
   const uint64_t row = blockIdx.x;
   // the tensor owning this row: last t with row_begin <= row
   uint32_t lo = 0, hi = a.num_tensors - 1;
@@ -272,6 +274,7 @@ __device__ __forceinline__ double row_sum(const uint32_t* r) {
 // one combine level: block b reduces rows [b*1024, min((b+1)*1024, nrows))
 __global__ void __launch_bounds__(kThreads)
     gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out) {
+  pdl_wait_then_release();
   const uint64_t r0 = (uint64_t)blockIdx.x * kFanIn;
   double s = 0.0;
   uint32_t c = 0;
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     gs_report_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ report,
                      uint32_t* __restrict__ host_copy) {
+  pdl_wait_then_release();
   double s = 0.0;
   uint32_t c = 0;
   for (uint64_t r = threadIdx.x; r < nrows; r += kThreads) {
@@ -445,6 +449,7 @@ __device__ __forceinline__ void update_one(float* const* P, int rep, const float
 // One launch per tensor (the pages' design).
 template <int REP>  // REP > 0: compile-time replica count; 0: runtime
 __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
+  pdl_wait_then_release();
   const int rep = REP > 0 ? REP : a.replicas;
   const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
   const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
@@ -462,6 +467,7 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
 template <int REP>
 __global__ void __launch_bounds__(kThreads)
     gs_update_multi_kernel(const __grid_constant__ GsMultiUpdateArgs a) {
+  pdl_wait_then_release();
   const int rep = REP > 0 ? REP : a.replicas;
   const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
   const uint64_t row = blockIdx.x;
@@ -497,6 +503,7 @@ __global__ void __launch_bounds__(kThreads)
 // host's computation.
 __global__ void gs_decide_kernel(const uint32_t* __restrict__ report, double max_norm,
                                  GsDecision* __restrict__ out) {
+  pdl_wait_then_release();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   const double sum_sq = row_sum(report);
   const double norm = sqrt(sum_sq);
@@ -524,47 +531,45 @@ int sm_count() {
 
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
   if (a.total_rows == 0) return cudaSuccess;
-  const dim3 grid((unsigned)a.total_rows);
+  const dim3 grid((unsigned)a.total_rows), block(kThreads);
   switch (a.R) {
-    case 1: gs::gs_stats_kernel<1><<<grid, kThreads, 0, stream>>>(a); break;
-    case 2: gs::gs_stats_kernel<2><<<grid, kThreads, 0, stream>>>(a); break;
-    case 4: gs::gs_stats_kernel<4><<<grid, kThreads, 0, stream>>>(a); break;
-    case 8: gs::gs_stats_kernel<8><<<grid, kThreads, 0, stream>>>(a); break;
-    default: gs::gs_stats_kernel<0><<<grid, kThreads, 0, stream>>>(a); break;
+    case 1: return launch_kernel(gs::gs_stats_kernel<1>, grid, block, 0, stream, a);
+    case 2: return launch_kernel(gs::gs_stats_kernel<2>, grid, block, 0, stream, a);
+    case 4: return launch_kernel(gs::gs_stats_kernel<4>, grid, block, 0, stream, a);
+    case 8: return launch_kernel(gs::gs_stats_kernel<8>, grid, block, 0, stream, a);
+    default: return launch_kernel(gs::gs_stats_kernel<0>, grid, block, 0, stream, a);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
                               cudaStream_t stream) {
   const unsigned blocks = (unsigned)((nrows + gs::kFanIn - 1) / gs::kFanIn);
-  gs::gs_combine_kernel<<<blocks, kThreads, 0, stream>>>(in, nrows, out);
-  return cudaGetLastError();
+  return launch_kernel(gs::gs_combine_kernel, dim3(blocks), dim3(kThreads), 0, stream, in, nrows,
+                       out);
 }
 
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
                              uint32_t* host_copy, cudaStream_t stream) {
-  gs::gs_report_kernel<<<1, kThreads, 0, stream>>>(in, nrows, report, host_copy);
-  return cudaGetLastError();
+  return launch_kernel(gs::gs_report_kernel, dim3(1), dim3(kThreads), 0, stream, in, nrows, report,
+                       host_copy);
 }
 
 cudaError_t launch_gs_update_multi(const GsMultiUpdateArgs& a, cudaStream_t stream) {
   if (a.total_rows == 0) return cudaSuccess;
-  const dim3 grid((unsigned)a.total_rows);
+  const dim3 grid((unsigned)a.total_rows), block(kThreads);
   switch (a.replicas) {
-    case 1: gs::gs_update_multi_kernel<1><<<grid, kThreads, 0, stream>>>(a); break;
-    case 2: gs::gs_update_multi_kernel<2><<<grid, kThreads, 0, stream>>>(a); break;
-    case 4: gs::gs_update_multi_kernel<4><<<grid, kThreads, 0, stream>>>(a); break;
-    case 8: gs::gs_update_multi_kernel<8><<<grid, kThreads, 0, stream>>>(a); break;
-    default: gs::gs_update_multi_kernel<0><<<grid, kThreads, 0, stream>>>(a); break;
+    case 1: return launch_kernel(gs::gs_update_multi_kernel<1>, grid, block, 0, stream, a);
+    case 2: return launch_kernel(gs::gs_update_multi_kernel<2>, grid, block, 0, stream, a);
+    case 4: return launch_kernel(gs::gs_update_multi_kernel<4>, grid, block, 0, stream, a);
+    case 8: return launch_kernel(gs::gs_update_multi_kernel<8>, grid, block, 0, stream, a);
+    default: return launch_kernel(gs::gs_update_multi_kernel<0>, grid, block, 0, stream, a);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_gs_decide(const uint32_t* report, double max_grad_norm, GsDecision* out,
                              cudaStream_t stream) {
-  gs::gs_decide_kernel<<<1, 32, 0, stream>>>(report, max_grad_norm, out);
-  return cudaGetLastError();
+  return launch_kernel(gs::gs_decide_kernel, dim3(1), dim3(32), 0, stream, report, max_grad_norm,
+                       out);
 }
 
 cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
@@ -574,14 +579,14 @@ cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
   const uint64_t cap = (uint64_t)gs::sm_count() * 64;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  const dim3 grid((unsigned)blocks), block(kThreads);
   switch (a.replicas) {
-    case 1: gs::gs_update_kernel<1><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
-    case 2: gs::gs_update_kernel<2><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
-    case 4: gs::gs_update_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
-    case 8: gs::gs_update_kernel<8><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
-    default: gs::gs_update_kernel<0><<<(unsigned)blocks, kThreads, 0, stream>>>(a); break;
+    case 1: return launch_kernel(gs::gs_update_kernel<1>, grid, block, 0, stream, a);
+    case 2: return launch_kernel(gs::gs_update_kernel<2>, grid, block, 0, stream, a);
+    case 4: return launch_kernel(gs::gs_update_kernel<4>, grid, block, 0, stream, a);
+    case 8: return launch_kernel(gs::gs_update_kernel<8>, grid, block, 0, stream, a);
+    default: return launch_kernel(gs::gs_update_kernel<0>, grid, block, 0, stream, a);
   }
-  return cudaGetLastError();
 }
 
 // ---- statistics without allocation -----------------------------------------
