@@ -449,7 +449,10 @@ __device__ __forceinline__ void update_one(float* const* P, int rep, const float
 // One launch per tensor (the pages' design).
 template <int REP>  // REP > 0: compile-time replica count; 0: runtime
 __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
-  pdl_wait_then_release();
+  // The next kernel is released only once this CTA's vectors are done: these
+  // kernels run on parallel chains, and CTAs released early would sit in SM
+  // slots waiting while the other chains' kernels need them.
+  pdl_wait();
   const int rep = REP > 0 ? REP : a.replicas;
   const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
   const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
@@ -457,6 +460,7 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
   const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
   for (uint64_t v = tid; v < nv; v += nthreads)
     if (!update_vec4<REP>(a.state, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
+  pdl_release();
   if (sv.d.skip) return;
   for (uint64_t i = nv * 4 + tid; i < a.numel; i += nthreads)
     update_one(a.state, rep, a.mean_grad, a.grads, a.R, i, sv);

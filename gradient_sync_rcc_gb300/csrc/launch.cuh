@@ -19,9 +19,13 @@
 
 namespace rcc {
 
-__device__ __forceinline__ void pdl_wait_then_release() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_then_release() {
+  pdl_wait();
+  pdl_release();
 }
 
 // RCC_PDL=0 launches without the attribute (plain stream order).
