@@ -59,10 +59,13 @@ inline int wait_limit_ms() {
 
 // Wait for an event with a time limit: poll, yield, then back off with short
 // sleeps.  Never blocks forever.
+// Polls with yields for the first 20 ms (a grad-sync readback waits for a
+// statistics pass of up to a few ms and sits on the step's critical path),
+// then sleeps 50 us between polls up to the limit.
 inline rcc_status wait_event(cudaEvent_t ev, const char* what) {
   const auto t0 = std::chrono::steady_clock::now();
   const int limit = wait_limit_ms();
-  for (long spins = 0;; ++spins) {
+  for (;;) {
     cudaError_t e = cudaEventQuery(ev);
     if (e == cudaSuccess) return RCC_OK;
     if (e != cudaErrorNotReady) return cuda_fail(e, what);
@@ -71,7 +74,7 @@ inline rcc_status wait_event(cudaEvent_t ev, const char* what) {
                         .count();
     if (ms > limit)
       return fail(RCC_ERR_TIMEOUT, "%s: GPU work did not complete within %d ms", what, limit);
-    if (spins < 2000)
+    if (ms < 20)
       std::this_thread::yield();
     else
       std::this_thread::sleep_for(std::chrono::microseconds(50));
