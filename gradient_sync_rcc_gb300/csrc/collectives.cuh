@@ -3,9 +3,11 @@
 // Replaces the ring schedule with host-staged transfers that the ruCCL README
 // describes (§5 "CUDA example", §6 data path) by a single pass over HBM: all R
 // rank buffers live on one GPU, so each output element is produced by one
-// thread that loads the element from every source rank (16-byte vectors,
-// coalesced, L1-bypassing streaming loads) and stores the result to every
-// destination (streaming stores).  Minimum traffic, no staging, no exchange.
+// thread that loads the element from every source rank (32-byte vectors where
+// every address allows, else 16-byte, else scalars; coalesced, L1-bypassing)
+// and stores the result to every destination (streaming stores).  Minimum
+// traffic, no staging, no exchange.  Launched with programmatic dependent
+// launch (launch.cuh).
 //
 // Arithmetic is fp32 for both element types (bf16 is widened exactly and the
 // result is rounded once to nearest-even).  Sums fold ranks in the order

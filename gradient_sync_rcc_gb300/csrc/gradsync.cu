@@ -11,14 +11,19 @@
 // skips the whole step; master weights and moments are FP32; the update is one
 // kernel per parameter, not one kernel for the whole model.
 //
-// Kernels:
+// Kernels (all launched with programmatic dependent launch, launch.cuh):
 //   gs_stats_kernel   all_reduce Mean of the R scaled gradients + unscale,
 //                     optional store of the mean gradient, and one 12-byte row
 //                     {sum g^2 (fp64), non-finite count (u32)} per block
 //   gs_combine_kernel one fan-in-1024 combine level: 1024 rows -> 1 row
-//   gs_report_kernel  the last <= 1024 rows (or all rows, flat) -> report
+//   gs_report_kernel  the last <= 1024 rows (or all rows, flat) -> report,
+//                     also stored to the host's mapped readback slot
+//   gs_decide_kernel  the host's skip / clip decision taken on the GPU (the
+//                     device-decision flows)
 //   gs_update_kernel  one launch per tensor: clip, decoupled decay, moments,
 //                     bias-corrected step on every optimizer-state replica
+//   gs_update_multi_kernel  the same update for every tensor in one launch
+//                     (a comparison flow)
 //
 // Row layout: three u32 words {low, high word of the fp64 sum, count}.
 #include <cuda_runtime.h>
