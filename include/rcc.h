@@ -33,6 +33,18 @@
  *     form.  Outputs must not overlap each other or any input otherwise.
  *   - The current CUDA device must be the session's device.
  *   - Error text for the calling thread: rcc_last_error_message().
+ *   - Kernels are launched with programmatic dependent launch: each waits
+ *     for the kernel ahead of it on the stream to finish before touching
+ *     memory, so ordering is that of a plain launch; only the launch latency
+ *     overlaps.  Streams captured into a CUDA graph record these as
+ *     programmatic edges.
+ *
+ * Environment (read once per process):
+ *   RCC_WAIT_LIMIT_MS  limit of every host wait (default 120000).
+ *   RCC_PDL=0          launch without programmatic dependent launch.
+ *   RCC_VEC_BYTES=16   cap vector accesses at 16 bytes.
+ * Built with -DRCC_BULK_COPY=1, the copy collectives go through shared
+ * memory with bulk copies instead of vector loads (slower; a comparison).
  */
 #ifndef RCC_H
 #define RCC_H
