@@ -57,11 +57,21 @@ inline int wait_limit_ms() {
   return 120000;
 }
 
-// Wait for an event with a time limit: poll, yield, then back off with short
-// sleeps.  Never blocks forever.
-// Polls with yields for the first 20 ms (a grad-sync readback waits for a
-// statistics pass of up to a few ms and sits on the step's critical path),
-// then sleeps 50 us between polls up to the limit.
+// Parallel chains of the per-tensor update launches: RCC_CHAINS (1..32),
+// default 16 (measured best with 24; 8 and 32 were slower).
+inline int chain_count() {
+  static const int n = [] {
+    const char* v = std::getenv("RCC_CHAINS");
+    const int k = v ? std::atoi(v) : 16;
+    return k < 1 ? 1 : (k > 32 ? 32 : k);
+  }();
+  return n;
+}
+
+// Wait for an event with a time limit; never blocks forever.  Polls with
+// yields for the first 20 ms (a grad-sync readback waits for a statistics pass
+// of up to a few ms and sits on the step's critical path), then sleeps 50 us
+// between polls up to the limit.
 inline rcc_status wait_event(cudaEvent_t ev, const char* what) {
   const auto t0 = std::chrono::steady_clock::now();
   const int limit = wait_limit_ms();
@@ -110,12 +120,13 @@ struct Scratch {
   rcc::AdamWScalars* scalars_dev = nullptr;
   rcc::AdamWScalars* scalars_host = nullptr;  // pinned staging
   rcc::GsDecision* decision_host = nullptr;   // pinned staging of a host decision
-  // captured update launches: a fork/join graph of kBranches parallel chains
-  static constexpr int kBranches = 8;
+  // per-tensor update launches on up to kMaxBranches parallel fork/join
+  // chains (chain_count() of them), also the shape of the captured graph
+  static constexpr int kMaxBranches = 32;
   cudaStream_t capture_stream = nullptr;
-  cudaStream_t branch[kBranches] = {};
+  cudaStream_t branch[kMaxBranches] = {};
   cudaEvent_t fork_ev = nullptr;
-  cudaEvent_t join_ev[kBranches] = {};
+  cudaEvent_t join_ev[kMaxBranches] = {};
   cudaGraphExec_t graph_exec = nullptr;
   uint64_t graph_gen = 0;           // desc_gen the graph was captured for
   size_t graph_P = 0;
@@ -192,7 +203,7 @@ inline void free_scratch(Scratch& s) {
   if (s.decision_host) cudaFreeHost(s.decision_host);
   if (s.graph_exec) cudaGraphExecDestroy(s.graph_exec);
   if (s.capture_stream) cudaStreamDestroy(s.capture_stream);
-  for (int k = 0; k < Scratch::kBranches; ++k) {
+  for (int k = 0; k < Scratch::kMaxBranches; ++k) {
     if (s.branch[k]) cudaStreamDestroy(s.branch[k]);
     if (s.join_ev[k]) cudaEventDestroy(s.join_ev[k]);
   }

@@ -357,11 +357,11 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   };
   auto enqueue_branched = [&](cudaStream_t origin) -> cudaError_t {
     cudaError_t le;
-    const int nb = (int)std::min<size_t>(P, Scratch::kBranches);
+    const int nb = (int)std::min<size_t>(P, (size_t)chain_count());
     if (nb == 1) return enqueue_one(0, origin);  // one tensor: no fork/join
     if (!sc.fork_ev && (le = cudaEventCreateWithFlags(&sc.fork_ev, cudaEventDisableTiming)))
       return le;
-    for (int k = 0; k < Scratch::kBranches; ++k) {
+    for (int k = 0; k < nb; ++k) {
       if (!sc.branch[k] &&
           (le = cudaStreamCreateWithFlags(&sc.branch[k], cudaStreamNonBlocking)) != cudaSuccess)
         return le;
@@ -383,8 +383,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     for (size_t p = 0; p < P; ++p) order[p] = p;
     std::stable_sort(order.begin(), order.end(),
                      [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
-    std::vector<size_t> chain[Scratch::kBranches];
-    uint64_t load[Scratch::kBranches] = {};
+    std::vector<size_t> chain[Scratch::kMaxBranches];
+    uint64_t load[Scratch::kMaxBranches] = {};
     for (size_t p : order) {
       int k = 0;
       for (int j = 1; j < nb; ++j)

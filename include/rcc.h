@@ -43,6 +43,8 @@
  *   RCC_WAIT_LIMIT_MS  limit of every host wait (default 120000).
  *   RCC_PDL=0          launch without programmatic dependent launch.
  *   RCC_VEC_BYTES=16   cap vector accesses at 16 bytes.
+ *   RCC_CHAINS=n       parallel chains of per-tensor update launches
+ *                      (1..32, default 16).
  * Built with -DRCC_BULK_COPY=1, the copy collectives go through shared
  * memory with bulk copies instead of vector loads (slower; a comparison).
  */
