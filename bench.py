@@ -390,7 +390,7 @@ def bench_ours(args):
                   for i, name in enumerate(ROWS)}
 
         # end to end: inputs from pinned host memory, result read back, every step
-        Ke = max(3, min(K, 20))
+        Ke = max(3, min(K, 50))
         barrier(world)
         e2e_ms = e2e_leg(torch, rcc, wl, h, Ke)
         barrier(world)

@@ -536,6 +536,19 @@ int sm_count() {
   return cached[dev];
 }
 
+// Copies `words` 32-bit words from pinned host memory mapped into the
+// device's address space, with SM loads instead of a copy engine: a small
+// table then does not queue behind large host<->device copies that the caller
+// has in flight on other streams.  The loads bypass the caches (ld.cv), since
+// the host rewrites the staging memory between calls.
+__global__ void __launch_bounds__(kThreads)
+    gs_upload_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst, uint64_t words) {
+  pdl_wait_then_release();
+  for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < words;
+       i += (uint64_t)gridDim.x * kThreads)
+    dst[i] = __ldcv(src + i);
+}
+
 }  // namespace gs
 
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
@@ -573,6 +586,17 @@ cudaError_t launch_gs_update_multi(const GsMultiUpdateArgs& a, cudaStream_t stre
     case 8: return launch_kernel(gs::gs_update_multi_kernel<8>, grid, block, 0, stream, a);
     default: return launch_kernel(gs::gs_update_multi_kernel<0>, grid, block, 0, stream, a);
   }
+}
+
+cudaError_t launch_host_upload(const void* src_mapped, void* dst, size_t bytes,
+                               cudaStream_t stream) {
+  const uint64_t words = bytes / 4;
+  uint64_t blocks = (words + kThreads - 1) / kThreads;
+  if (blocks > 64) blocks = 64;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(gs::gs_upload_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream,
+                       static_cast<const uint32_t*>(src_mapped), static_cast<uint32_t*>(dst),
+                       words);
 }
 
 cudaError_t launch_gs_decide(const uint32_t* report, double max_grad_norm, GsDecision* out,

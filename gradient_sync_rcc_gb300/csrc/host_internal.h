@@ -108,7 +108,8 @@ struct Scratch {
                                         // null: then a 12-byte D2H copy fills the slot
   void* desc_dev = nullptr;         // tensor table + grad table + state table
   size_t desc_cap = 0;
-  void* desc_host = nullptr;        // pinned staging for the tables
+  void* desc_host = nullptr;        // pinned, mapped staging for the tables
+  void* desc_host_dev = nullptr;    // its device alias (null: copied by DMA)
   size_t desc_host_cap = 0;
   std::vector<unsigned char> last_desc;  // bytes most recently uploaded
   cudaEvent_t report_ev = nullptr;
@@ -118,8 +119,10 @@ struct Scratch {
   // device decision
   rcc::GsDecision* decision_dev = nullptr;
   rcc::AdamWScalars* scalars_dev = nullptr;
-  rcc::AdamWScalars* scalars_host = nullptr;  // pinned staging
-  rcc::GsDecision* decision_host = nullptr;   // pinned staging of a host decision
+  rcc::AdamWScalars* scalars_host = nullptr;  // pinned, mapped staging
+  rcc::AdamWScalars* scalars_host_dev = nullptr;
+  rcc::GsDecision* decision_host = nullptr;   // pinned, mapped staging of a host decision
+  rcc::GsDecision* decision_host_dev = nullptr;
   // per-tensor update launches on up to kMaxBranches parallel fork/join
   // chains (chain_count() of them), also the shape of the captured graph
   static constexpr int kMaxBranches = 32;

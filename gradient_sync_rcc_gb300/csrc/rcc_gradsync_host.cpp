@@ -22,6 +22,36 @@ rcc_status ensure_dev(T** p, size_t* cap, size_t need, const char* what) {
   return RCC_OK;
 }
 
+// Pinned host staging mapped into the device's address space; *alias is
+// null when no device alias can be had (the upload then goes by DMA).
+template <typename T>
+cudaError_t alloc_mapped(T** host, T** alias, size_t bytes) {
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(host), bytes, cudaHostAllocMapped);
+  if (e != cudaSuccess) return e;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, *host, 0) == cudaSuccess)
+    *alias = static_cast<T*>(d);
+  else
+    (void)cudaGetLastError();
+  return cudaSuccess;
+}
+
+// Host staging -> device memory on `cs`.  A small kernel reads the staging
+// through its device alias: a copy-engine transfer would queue behind large
+// host<->device copies that the caller may have in flight on other streams
+// (a 64 MiB transfer holds a 4 KB table back by about 0.3 ms).
+static_assert(sizeof(rcc::AdamWScalars) % 4 == 0 && sizeof(rcc::GsDecision) % 4 == 0,
+              "uploads move whole 32-bit words");
+static_assert(sizeof(rcc::GsTensor) % 8 == 0, "descriptor tables are whole 64-bit words");
+
+cudaError_t upload(void* dst, const void* host, const void* alias, size_t bytes, cudaStream_t cs) {
+  if (alias) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return rcc::launch_host_upload(alias, dst, bytes, cs);
+  }
+  return cudaMemcpyAsync(dst, host, bytes, cudaMemcpyHostToDevice, cs);
+}
+
 rcc_status ensure_fixed_scratch(Scratch& sc) {
   cudaError_t e;
   if (!sc.combine) {
@@ -65,12 +95,12 @@ rcc_status ensure_decision_scratch(Scratch& sc) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scalars)");
   }
   if (!sc.scalars_host) {
-    e = cudaMallocHost(reinterpret_cast<void**>(&sc.scalars_host), sizeof(rcc::AdamWScalars));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(scalars)");
+    e = alloc_mapped(&sc.scalars_host, &sc.scalars_host_dev, sizeof(rcc::AdamWScalars));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(scalars)");
   }
   if (!sc.decision_host) {
-    e = cudaMallocHost(reinterpret_cast<void**>(&sc.decision_host), sizeof(rcc::GsDecision));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(decision)");
+    e = alloc_mapped(&sc.decision_host, &sc.decision_host_dev, sizeof(rcc::GsDecision));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(decision)");
   }
   return RCC_OK;
 }
@@ -200,8 +230,9 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   if (!sc.desc_host || sc.desc_host_cap < desc_bytes) {
     if (sc.desc_host) cudaFreeHost(sc.desc_host);
     sc.desc_host = nullptr;
-    cudaError_t e = cudaMallocHost(&sc.desc_host, desc_bytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocHost(descriptors)");
+    sc.desc_host_dev = nullptr;
+    cudaError_t e = alloc_mapped(&sc.desc_host, &sc.desc_host_dev, desc_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(descriptors)");
     sc.desc_host_cap = desc_bytes;
   }
   std::vector<unsigned char> desc(desc_bytes);
@@ -275,7 +306,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   }
   if (dev_grew || sc.last_desc != desc) {
     std::memcpy(sc.desc_host, desc.data(), desc_bytes);
-    e = cudaMemcpyAsync(sc.desc_dev, sc.desc_host, desc_bytes, cudaMemcpyHostToDevice, cs);
+    e = upload(sc.desc_dev, sc.desc_host, sc.desc_host_dev, desc_bytes, cs);
     if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
     sc.last_desc.swap(desc);
     ++sc.desc_gen;
@@ -289,8 +320,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     if ((st = ensure_decision_scratch(sc)) != RCC_OK) return st;
     *sc.scalars_host = step_scalars(cfg, t_next);
     sc.scalars_host->inv_scale = (float)(1.0 / state->scale);
-    e = cudaMemcpyAsync(sc.scalars_dev, sc.scalars_host, sizeof(rcc::AdamWScalars),
-                        cudaMemcpyHostToDevice, cs);
+    e = upload(sc.scalars_dev, sc.scalars_host, sc.scalars_host_dev, sizeof(rcc::AdamWScalars),
+               cs);
     if (e != cudaSuccess) return cuda_fail(e, "scalar upload");
   }
   const char* dbase = static_cast<const char*>(sc.desc_dev);
@@ -530,8 +561,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       // the host's decision goes to device memory for the replayed graph
       sc.decision_host->skip = 0u;
       sc.decision_host->coef = coef;
-      if ((e = cudaMemcpyAsync(sc.decision_dev, sc.decision_host, sizeof(rcc::GsDecision),
-                               cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+      if ((e = upload(sc.decision_dev, sc.decision_host, sc.decision_host_dev,
+                      sizeof(rcc::GsDecision), cs)) != cudaSuccess)
         return cuda_fail(e, "decision upload");
       if ((st = replay_graph()) != RCC_OK) return st;
     } else {

@@ -86,6 +86,10 @@ cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);
 // One fan-in-1024 combine level: ceil(nrows / 1024) output rows.
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
                               cudaStream_t stream);
+// Copies `bytes` (a multiple of 4) from pinned host memory, given by its
+// device alias, to device memory with a kernel (no copy engine).
+cudaError_t launch_host_upload(const void* src_mapped, void* dst, size_t bytes,
+                               cudaStream_t stream);
 // Final reduction of nrows rows into the 12-byte report (one block); the
 // same 12 bytes also go to `host_copy` (a mapped pinned slot) when non-null.
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
