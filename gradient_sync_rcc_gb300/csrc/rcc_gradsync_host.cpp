@@ -389,7 +389,11 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   auto enqueue_branched = [&](cudaStream_t origin) -> cudaError_t {
     cudaError_t le;
     const int nb = (int)std::min<size_t>(P, (size_t)chain_count());
-    if (nb == 1) return enqueue_one(0, origin);  // one tensor: no fork/join
+    if (nb == 1) {  // one chain (one tensor, or RCC_CHAINS=1): no fork/join
+      for (size_t p = 0; p < P; ++p)
+        if ((le = enqueue_one(p, origin)) != cudaSuccess) return le;
+      return cudaSuccess;
+    }
     if (!sc.fork_ev && (le = cudaEventCreateWithFlags(&sc.fork_ev, cudaEventDisableTiming)))
       return le;
     for (int k = 0; k < nb; ++k) {

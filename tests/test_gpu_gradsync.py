@@ -364,3 +364,32 @@ def test_rank_counts_that_are_not_powers_of_two(orc, R, mean_grad):
     sizes = [5000, 1023, 64]
     prob = Problem(R, sizes, 17, 1, mean_grad)
     run_steps(orc, prob, 3, None, {})
+
+
+_CHAIN_CHECK = """
+import sys
+sys.path.insert(0, {tests!r})
+import oracle
+oracle.build.build()
+import test_gpu_gradsync as t
+from gradient_sync_rcc_gb300 import rcc, synth
+for flags in (0, rcc.ADAMW_GRAPH, rcc.ADAMW_HOST_GRAPH):
+    prob = t.Problem(4, synth.param_sizes(9, 1024, 40000, 17), 18, 1, True)
+    t.run_steps(oracle, prob, 3, None, {{"flags": flags}})
+print("chains ok")
+"""
+
+
+@pytest.mark.parametrize("chains", ["1", "3"])
+def test_chain_counts_update_every_tensor(chains):
+    """The chain count is read once per process (RCC_CHAINS), so other counts
+    run in a child process: every tensor must still be updated, in every
+    per-tensor flow."""
+    import os
+    import subprocess
+    import sys
+    tests = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, RCC_CHAINS=chains)
+    out = subprocess.run([sys.executable, "-c", _CHAIN_CHECK.format(tests=tests)], env=env,
+                         cwd=os.path.dirname(tests), capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0 and "chains ok" in out.stdout, out.stdout + out.stderr
