@@ -393,3 +393,27 @@ def test_chain_counts_update_every_tensor(chains):
     out = subprocess.run([sys.executable, "-c", _CHAIN_CHECK.format(tests=tests)], env=env,
                          cwd=os.path.dirname(tests), capture_output=True, text=True, timeout=600)
     assert out.returncode == 0 and "chains ok" in out.stdout, out.stdout + out.stderr
+
+
+@pytest.mark.parametrize("off", [1, 4, 8])
+@pytest.mark.parametrize("mode", ["host", "device_multi"])
+def test_misaligned_tensors(orc, off, mode):
+    """Every buffer a view `off` floats into a larger allocation: 4 bytes
+    (scalar paths), 16 bytes (16-byte vectors) or 32 bytes (32-byte statistics
+    vectors) past a 256-byte boundary."""
+    sizes = [5000, 1027, 64, 8195]
+    prob = Problem(4, sizes, 19, 1, True)
+
+    def shift(t):
+        base = torch.empty(t.numel() + off, device=DEV)
+        v = base[off:off + t.numel()]
+        v.copy_(t)
+        return v
+
+    for t in prob.tensors:
+        t["grads"] = [shift(g) for g in t["grads"]]
+        for key in ("params", "exp_avg", "exp_avg_sq"):
+            t[key] = [shift(x) for x in t[key]]
+        t["mean_grad"] = shift(t["mean_grad"])
+    prob.sets = rcc.ParamSets(prob.tensors)
+    run_steps(orc, prob, 3, None, {"flags": MODES[mode]})
