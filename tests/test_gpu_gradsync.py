@@ -358,12 +358,17 @@ def test_overlapping_outputs_rejected_shared_grads_allowed():
 
 @pytest.mark.parametrize("R", [3, 6])
 @pytest.mark.parametrize("mean_grad", [True, False])
-def test_rank_counts_that_are_not_powers_of_two(orc, R, mean_grad):
+@pytest.mark.parametrize("per_rank_state", [False, True])
+def test_rank_counts_that_are_not_powers_of_two(orc, R, mean_grad, per_rank_state):
     """R = 3 and 6 divide (no exact reciprocal); with no stored mean gradient
-    the update recomputes the mean with the same arithmetic."""
+    the update recomputes the mean with the same arithmetic.  With R state
+    copies the update kernels take their runtime replica-count path."""
     sizes = [5000, 1023, 64]
-    prob = Problem(R, sizes, 17, 1, mean_grad)
+    prob = Problem(R, sizes, 17, R if per_rank_state else 1, mean_grad)
     run_steps(orc, prob, 3, None, {})
+    if per_rank_state:
+        prob2 = Problem(R, sizes, 17, R, mean_grad)
+        run_steps(orc, prob2, 2, None, {"flags": MODES["device_multi"]})
 
 
 _CHAIN_CHECK = """
