@@ -115,6 +115,9 @@ struct Scratch {
   cudaEvent_t report_ev = nullptr;
   cudaEvent_t done_ev = nullptr;    // end of the previous call's work
   bool done_recorded = false;
+  // a call gave up waiting for its report: its GPU work (which reads the host
+  // staging and the tables) may still be pending, up to done_ev
+  bool stale = false;
   uint64_t desc_gen = 0;            // bumped at every descriptor upload
   // device decision
   rcc::GsDecision* decision_dev = nullptr;

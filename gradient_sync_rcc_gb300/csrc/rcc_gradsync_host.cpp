@@ -213,6 +213,12 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   std::lock_guard<std::mutex> lock(s->mu);
   Scratch& sc = s->sc;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (sc.stale) {
+    // the previous call timed out with work still queued that reads the
+    // staging memory and tables rewritten below: let it finish first
+    if ((st = wait_event(sc.done_ev, "the previous call's GPU work")) != RCC_OK) return st;
+    sc.stale = false;
+  }
   if ((st = ensure_fixed_scratch(sc)) != RCC_OK) return st;
   if ((st = ensure_dev(&sc.rows, &sc.rows_cap, (size_t)total_rows * 12, "cudaMalloc(rows)")) !=
       RCC_OK)
@@ -524,7 +530,15 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     device_updates = launches_per_update;
     g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
   }
-  if ((st = wait_event(sc.report_ev, "12-byte report readback")) != RCC_OK) return st;
+  if ((st = wait_event(sc.report_ev, "12-byte report readback")) != RCC_OK) {
+    // nothing of this step is applied by the host (default flow: no update
+    // was launched); mark the queued work so that the next call waits for it
+    if (cudaEventRecord(sc.done_ev, cs) == cudaSuccess) {
+      sc.done_recorded = true;
+      sc.stale = true;
+    }
+    return st;
+  }
 
   // the decision [RUDA docs, native PyTorch section]: skip on non-finite,
   // clip after unscale when the global norm exceeds max_grad_norm

@@ -319,7 +319,12 @@ typedef struct {
  * mean-gradient buffers must not overlap any other buffer of the call
  * (RCC_ERR_INVALID_ARGUMENT; checked whenever the set of buffers changes).
  * `state` is read and updated; `report` (may be NULL) receives what happened.
- * Returns RCC_ERR_TIMEOUT if the report did not arrive within the wait limit. */
+ * Returns RCC_ERR_TIMEOUT if the report did not arrive within the wait limit:
+ * in the default and RCC_ADAMW_HOST_GRAPH flows nothing is then applied and
+ * `state` is unchanged (the call may simply be repeated); in the
+ * device-decision flows the queued updates still run, so the optimizer state
+ * should be treated as unknown.  The next call on the session first waits
+ * (bounded) for the abandoned call's queued work. */
 rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params,
                                int num_params, const rcc_adamw_cfg* cfg,
                                rcc_optim_state* state, rcc_step_report* report,

@@ -422,3 +422,42 @@ def test_misaligned_tensors(orc, off, mode):
         t["mean_grad"] = shift(t["mean_grad"])
     prob.sets = rcc.ParamSets(prob.tensors)
     run_steps(orc, prob, 3, None, {"flags": MODES[mode]})
+
+
+def test_readback_timeout_applies_nothing_and_the_next_call_steps(orc, monkeypatch):
+    """A report that does not come back within RCC_WAIT_LIMIT_MS: the call
+    returns RCC_ERR_TIMEOUT with nothing applied (the default flow launches no
+    update before its decision) and the optimizer state unchanged.  The next
+    call waits for the queued work of the abandoned one before reusing its
+    staging memory, then steps exactly as the oracle does."""
+    sizes = [200000, 5000]
+    prob = Problem(4, sizes, 23, 1, True)
+    cfg = rcc.adamw_cfg(lr=LR, betas=(B1, B2), eps=EPS, weight_decay=WD, max_grad_norm=MAXN,
+                        replicas=1)
+    state = rcc.optim_state(scale=65536.0)
+    grads = prob.host_grads(1, state.scale)
+    prob.load_grads(grads)
+    p_before = [to_host(t["params"][0]) for t in prob.tensors]
+    busy = torch.empty(1 << 28, device=DEV)
+    busy.fill_(1.0)
+    with session(4) as h:
+        torch.cuda.synchronize()
+        for _ in range(40):                  # tens of ms of work ahead on the stream
+            busy.mul_(1.0)
+        monkeypatch.setenv("RCC_WAIT_LIMIT_MS", "1")
+        with pytest.raises(rcc.RccError) as err:
+            rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+        assert err.value.status == rcc.ERR_TIMEOUT
+        assert state.step == 0 and state.scale == 65536.0
+        monkeypatch.delenv("RCC_WAIT_LIMIT_MS")
+        torch.cuda.synchronize()
+        for i, t in enumerate(prob.tensors):
+            assert bits_equal(to_host(t["params"][0]), p_before[i])
+        rep = rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+        torch.cuda.synchronize()
+    assert rep.skipped == 0 and state.step == 1
+    sc = orc.scaler_new(65536.0)
+    orc.grad_sync_adamw_step(grads, prob.hp, prob.hm, prob.hv, lr=LR, beta1=B1, beta2=B2,
+                             eps=EPS, weight_decay=WD, max_grad_norm=MAXN, step=0, scaler=sc)
+    for i in range(len(sizes)):
+        assert close(to_host(prob.tensors[i]["params"][0]), prob.hp[i])
