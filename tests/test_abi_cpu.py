@@ -298,6 +298,8 @@ def test_grad_sync_validation(L, comm):
 
     arr, keep = _param_sets(L, R, R)
     assert reached_device_check(L, gs(arr))
+    empty, keepe = _param_sets(L, R, R, numel=0)
+    assert gs(empty) == L.ERR_INVALID_ARGUMENT and "0 elements" in L.last_error()
     assert gs(arr, P=0) == L.ERR_INVALID_ARGUMENT
     assert gs(arr, h=0x4242) == L.ERR_MISSING_REGISTRATION
     arr2, keep2 = _param_sets(L, R, R, rank_numel=[1000, 1000, 999, 1000])
