@@ -57,6 +57,16 @@ inline int wait_limit_ms() {
   return 120000;
 }
 
+// The default grad-sync flow replays its per-tensor update launches from a
+// captured graph once the same tensors come back (RCC_AUTO_GRAPH=0: never).
+inline bool auto_graph_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("RCC_AUTO_GRAPH");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // Parallel chains of the per-tensor update launches: RCC_CHAINS (1..32),
 // default 16 (measured best with 24; 8 and 32 were slower).
 inline int chain_count() {
@@ -119,6 +129,7 @@ struct Scratch {
   // staging and the tables) may still be pending, up to done_ev
   bool stale = false;
   uint64_t desc_gen = 0;            // bumped at every descriptor upload
+  uint64_t same_tables = 0;         // consecutive calls with unchanged tables
   // device decision
   rcc::GsDecision* decision_dev = nullptr;
   rcc::AdamWScalars* scalars_dev = nullptr;

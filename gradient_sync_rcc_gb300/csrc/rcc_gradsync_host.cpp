@@ -316,9 +316,20 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
     sc.last_desc.swap(desc);
     ++sc.desc_gen;
+    sc.same_tables = 0;
+  } else {
+    ++sc.same_tables;
   }
   const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
-  const bool host_graph = (cfg->flags & RCC_ADAMW_HOST_GRAPH) != 0;
+  // The default flow becomes the host-graph flow -- the same decision on the
+  // host, the same kernels, the P launches replayed from a captured graph --
+  // once the same tensors have come three calls in a row, for P >= 32 (below
+  // that the host's launches keep pace with the GPU).
+  constexpr size_t kAutoGraphMinTensors = 32;
+  const bool host_graph =
+      (cfg->flags & RCC_ADAMW_HOST_GRAPH) != 0 ||
+      (cfg->flags == 0 && P >= kAutoGraphMinTensors && sc.same_tables >= 2 &&
+       auto_graph_enabled());
   const int64_t t_next = state->step + 1;
   if (on_device || host_graph) {
     // the scalars of step t+1, read by the updates from device memory; used

@@ -45,6 +45,8 @@
  *   RCC_VEC_BYTES=16   cap vector accesses at 16 bytes.
  *   RCC_CHAINS=n       parallel chains of per-tensor update launches
  *                      (1..32, default 16).
+ *   RCC_AUTO_GRAPH=0   the default grad-sync flow never switches to graph
+ *                      replay.
  * Built with -DRCC_BULK_COPY=1, the copy collectives go through shared
  * memory with bulk copies instead of vector loads (slower; a comparison).
  */
@@ -251,7 +253,10 @@ typedef struct {
 } rcc_adamw_cfg;
 
 /* rcc_adamw_cfg.flags.  By default the call reads the 12-byte report back,
- * decides on the host, then launches the updates ([RUDA-T]).
+ * decides on the host, then launches the updates ([RUDA-T]).  Once the same
+ * tensors (32 or more) come three calls in a row, the default flow replays
+ * those launches from a captured graph, as RCC_ADAMW_HOST_GRAPH does
+ * (RCC_AUTO_GRAPH=0 keeps plain launches); the results are the same bits.
  * RCC_ADAMW_DEVICE_DECISION: one more kernel takes the same decision on the
  *   GPU from the report (identical arithmetic: IEEE double sqrt and division,
  *   one rounding to fp32), so the per-tensor updates are enqueued right behind
