@@ -405,6 +405,22 @@ inline int vec_ok(const MultiPtrArgs& a, int nsrc_ptrs, int ndst_ptrs, size_t se
   return 0;
 }
 
+// Sets a.vec_ok and a.stage for segments at offsets that are multiples of
+// seg_bytes.  When those offsets break a 16-byte alignment that the base
+// addresses have, the staged kernels align `side` within each segment instead
+// of falling back to scalar accesses everywhere.
+inline void set_layout(MultiPtrArgs& a, int nsrc_ptrs, int ndst_ptrs, size_t seg_bytes,
+                       rcc::Stage side) {
+  const int full = vec_ok(a, nsrc_ptrs, ndst_ptrs, seg_bytes, 0);
+  const int base = vec_ok(a, nsrc_ptrs, ndst_ptrs, 0, 0);
+  a.stage = rcc::kStageNone;
+  a.vec_ok = full;
+  if (full < 16 && base >= 16) {
+    a.vec_ok = base;
+    a.stage = side;
+  }
+}
+
 // The session is gone: every rank waiting in a per-rank collective returns
 // RCC_ERR_MISSING_REGISTRATION.
 inline void wake_waiters(Session& s) {

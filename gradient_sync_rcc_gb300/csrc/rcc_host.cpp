@@ -351,7 +351,7 @@ rcc_status reduce_scatter_impl(rcc_comm comm, const void* const* send, void* con
   a.src_seg_stride = n;
   a.dst_per_seg = 1;
   a.mean_div = ops[0] == RCC_MEAN ? R : 0;
-  a.vec_ok = vec_ok(a, R, R, n * es, 0);
+  set_layout(a, R, R, n * es, rcc::kStageSources);
   return launch(*s, red_of(ops[0]), R, a, stream, sync);
 }
 }  // namespace host
@@ -407,7 +407,7 @@ rcc_status all_gather_impl(rcc_comm comm, const void* const* send, void* const* 
   a.ndst = R;
   a.src_per_seg = 1;
   a.dst_seg_stride = n;
-  a.vec_ok = vec_ok(a, R, R, 0, n * es);
+  set_layout(a, R, R, n * es, rcc::kStageDestinations);
   return launch(*s, rcc::kRedCopy, R, a, stream, sync);
 }
 }  // namespace host
@@ -464,7 +464,7 @@ rcc_status rcc_all_to_all_single(rcc_comm comm, const void* const* send, void* c
   a.nsrc = 1;
   a.ndst = 1;
   a.a2a_ranks = R;
-  a.vec_ok = vec_ok(a, R, R, n * es, 0);
+  set_layout(a, R, R, n * es, rcc::kStageDestinations);
   return launch(*s, rcc::kRedCopy, R * R, a, stream);
 }
 

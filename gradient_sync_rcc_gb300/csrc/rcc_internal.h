@@ -44,8 +44,16 @@ struct MultiPtrArgs {
   int mean_div;  // > 0: the sum is divided by this (IEEE division) before storing
   int vec_ok;    // alignment class in bytes (0, 16 or 32): every source and
                  // destination address, with segment offsets, is a multiple of
-                 // it, so vectors of that many bytes may be used
+                 // it, so vectors of that many bytes may be used; with a
+                 // `stage`, only the base addresses are
+  int stage;     // kStageNone, or which side is aligned per segment (below)
 };
+
+// Segment offsets that are not vector-aligned while the base addresses are:
+// kStageSources aligns the sources of each segment (reductions: vector loads,
+// stores staged through shared memory); kStageDestinations aligns the
+// destinations (copies: loads staged through shared memory, vector stores).
+enum Stage : int { kStageNone = 0, kStageSources = 1, kStageDestinations = 2 };
 
 // One launch of the pass; fast selects the pairwise-tree sum.
 cudaError_t launch_multi_ptr_f32(Red red, bool fast, int nseg, const MultiPtrArgs& a,
