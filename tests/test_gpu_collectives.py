@@ -333,7 +333,10 @@ def test_special_values_max_min_sum(orc):
         assert bits_equal(to_host(outs[0]), orc.reduce_bf16(xb, op))
 
 
-@pytest.mark.parametrize("R,n", [(3, 257), (4, 1), (8, 4096), (5, 33), (64, 40)])
+# shards whose offsets s*n break 16-byte alignment go through the staged
+# kernels; the large ones there cover many full tiles plus head and tail
+@pytest.mark.parametrize("R,n", [(3, 257), (4, 1), (8, 4096), (5, 33), (64, 40),
+                                 (8, 262145), (3, 100003), (12, 65537), (4, 131074)])
 @pytest.mark.parametrize("dtype", [rcc.F32, rcc.BF16])
 def test_reduce_scatter_all_gather_shapes(orc, R, n, dtype):
     td = tdtype(dtype)
@@ -352,6 +355,32 @@ def test_reduce_scatter_all_gather_shapes(orc, R, n, dtype):
         assert rs[r].guards_intact() and ag[r].guards_intact()
         assert bits_equal(to_host(rs[r].t), want[r])
         assert bits_equal(to_host(ag[r].t), np.concatenate(want))
+
+
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("det", [True, False])
+def test_reduce_scatter_odd_shards_every_op(orc, op, det):
+    """The staged reduction at an odd shard, each op, both summation modes."""
+    R, n = 8, 65537
+    N = R * n
+    xs = host_ranks("uniform", R, N, 1101, R, n)
+    ins = [to_dev(x) for x in xs]
+    rs = [Guarded(n, torch.float32) for _ in range(R)]
+    with session(R, rcc.F32, det) as h:
+        rcc.reduce_scatter(h, ins, [g.t for g in rs], op)
+        torch.cuda.synchronize()
+    want = orc.reduce_scatter(xs, op)
+    exact = np.sum([x.astype(np.float64) for x in xs], axis=0)
+    mag = np.sum([np.abs(x.astype(np.float64)) for x in xs], axis=0)
+    for r in range(R):
+        assert rs[r].guards_intact()
+        got = to_host(rs[r].t)
+        if det or op != "sum":
+            assert bits_equal(got, want[r])
+        else:                                  # pairwise tree: within the fp32 bound
+            lo, hi = r * n, (r + 1) * n
+            assert np.all(np.abs(got.astype(np.float64) - exact[lo:hi])
+                          <= R * 2.0 ** -23 * mag[lo:hi])
 
 
 def test_all_gather_in_place(orc):
@@ -400,7 +429,8 @@ def test_finish_then_reregister_and_reset_with_pending_work():
 
 # ---------------------------------------------------------------- all_to_all_single, list all_gather
 
-@pytest.mark.parametrize("R,n", [(1, 100), (2, 4099), (3, 257), (4, 1 << 16), (8, 33), (8, 1 << 18)])
+@pytest.mark.parametrize("R,n", [(1, 100), (2, 4099), (3, 257), (4, 1 << 16), (8, 33), (8, 1 << 18),
+                                 (8, 262145), (4, 65539)])
 @pytest.mark.parametrize("dtype", [rcc.F32, rcc.BF16])
 def test_all_to_all_single(orc, R, n, dtype):
     td = tdtype(dtype)
