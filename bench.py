@@ -142,7 +142,7 @@ def peak_hbm():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("collectives.cuh", "collectives_f32.cu"):
+    for f in ("collectives.cuh", "collectives_part.cu"):
         with open(os.path.join(ROOT, "gradient_sync_rcc_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

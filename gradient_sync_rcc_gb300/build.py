@@ -19,8 +19,12 @@ NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["collectives_f32.cu", "collectives_bf16.cu", "gradsync.cu", "rcc_host.cpp",
-           "rcc_rank.cpp", "rcc_gradsync_host.cpp"]
+SOURCES = ["gradsync.cu", "rcc_host.cpp", "rcc_rank.cpp", "rcc_gradsync_host.cpp"]
+# collectives_part.cu is compiled once per (element type, reduction, tree
+# order) that the host dispatcher names: fp32 (0) and bf16 (1) x rank-order
+# sum (0), tree sum (0, fast), max (1), min (2), copy (3).
+PARTS = [(dt, red, fast) for dt in (0, 1)
+         for red, fast in ((0, 0), (0, 1), (1, 0), (2, 0), (3, 0))]
 
 
 def _inputs():
@@ -37,21 +41,34 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=(), lib: str = LIB,
+          objdir: str = OBJDIR) -> str:
+    """Compile librcc.so.  `defines` (e.g. ["-DRCC_WAVES=8"]) rebuild the
+    kernels with other tuning macros into `lib` / `objdir` (a comparison
+    build that RCC_LIBRARY can point the binding at)."""
+    defines = list(defines)
+    if not force and not defines and lib == LIB and up_to_date():
         return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
+    jobs = []
+    for dt, red, fast in PARTS:
+        name = "collectives_part_%d_%d_%d" % (dt, red, fast)
+        jobs.append((name, "collectives_part.cu",
+                     ["-DRCC_PART_DT=%d" % dt, "-DRCC_PART_RED=%d" % red,
+                      "-DRCC_PART_FAST=%d" % fast]))
+    for src in SOURCES:
+        jobs.append((os.path.splitext(src)[0], src, []))
     procs = []
     objs = []
-    for src in SOURCES:
-        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
+    for name, src, defs in jobs:
+        obj = os.path.join(objdir, name + ".o")
         objs.append(obj)
-        cmd = [NVCC, *ARCH, *COMMON, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [NVCC, *ARCH, *COMMON, *defines, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cpp"):
             cmd = [NVCC, *COMMON, "-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd))
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+        procs.append((name, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     failed = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -62,14 +79,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError("librcc build failed:\n" + msg)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     link = [NVCC, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
             "-Xlinker", "--version-script=" + os.path.join(CSRC, "exports.map")]
     if verbose:
         print(" ".join(link))
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -4,7 +4,7 @@
 // describes (§5 "CUDA example", §6 data path) by a single pass over HBM: all R
 // rank buffers live on one GPU, so each output element is produced by one
 // thread that loads the element from every source rank (32-byte vectors where
-// every address allows, else 16-byte, else scalars; coalesced, L1-bypassing)
+// every address allows, else 16-byte, else scalars; coalesced, no L1 allocation)
 // and stores the result to every destination (streaming stores).  Minimum
 // traffic, no staging, no exchange.  Launched with programmatic dependent
 // launch (launch.cuh).
@@ -15,7 +15,9 @@
 // the sum by R with an IEEE division; max/min keep the lowest rank among
 // equals and turn any NaN into the quiet NaN 0x7FC00000.
 //
-// Included by collectives_f32.cu and collectives_bf16.cu, one element type each.
+// Included by collectives_part.cu, which the build compiles once per element
+// type and reduction (launch_part below), so that the instantiations build in
+// parallel.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -40,19 +42,23 @@ struct Vec {
   uint32_t w[W];
 };
 
-// Streaming load through the non-coherent path without L1 allocation: every
-// input element is read exactly once.  Volatile keeps the loads and stores of
-// one thread in program order (in-place all_reduce reads an element before the
-// same thread overwrites it).
+// Source loads without L1 allocation: every input element is read exactly
+// once.  They take the coherent path, not the non-coherent (read-only) one,
+// which would be valid only while no thread of the kernel writes the data: a
+// destination may alias a source (in-place all_reduce, reduce and
+// all_gather).  On GB300 the two measured the same (8 ranks x 2^24 fp32 and
+// 2^26 bf16, every collective, within 0.5%).  Volatile keeps the loads and
+// stores of one thread in program order (an in-place element is read before
+// the same thread overwrites it).
 template <int W>
 __device__ __forceinline__ Vec<W> ld_vec(const void* p) {
   Vec<W> v;
   if constexpr (W == 4) {
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "l"(p));
   } else {
-    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
                    "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
                  : "l"(p));
@@ -657,158 +663,6 @@ inline int resident_blocks(const void* fn) {
   return per_sm;
 }
 
-// ---- bulk-copy (TMA) pass for the pure copies ------------------------------------
-// broadcast, all_gather, the list all_gather and all_to_all move bytes only.
-// Here one elected thread per CTA streams tiles through shared memory with the
-// bulk-copy engine: cp.async.bulk loads a tile (completion counted on an
-// mbarrier) and cp.async.bulk stores the same tile to every destination, so
-// the data never passes through registers.  Requires 16-byte aligned
-// addresses and a segment length that is a multiple of 16 bytes (the host
-// checks; otherwise the vector pass runs).  Every mbarrier wait is bounded:
-// if a tile never arrives the CTA raises its timeout flag, drains its stores
-// and returns.
-#ifndef RCC_BULK_TILE
-#define RCC_BULK_TILE 16384
-#endif
-#ifndef RCC_BULK_STAGES
-#define RCC_BULK_STAGES 4
-#endif
-#ifndef RCC_BULK_COPY
-#define RCC_BULK_COPY 0
-#endif
-constexpr int kBulkTile = RCC_BULK_TILE;
-constexpr int kBulkStages = RCC_BULK_STAGES;
-constexpr uint32_t kBulkSpinLimit = 1u << 24;
-
-// raised (never cleared on the device) when a bounded wait gave up
-static __device__ uint32_t g_bulk_timeout;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-template <int EB>
-__global__ void __launch_bounds__(32) bulk_copy_kernel(const __grid_constant__ MultiPtrArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t bars[kBulkStages];
-  pdl_wait_then_release();
-  if (threadIdx.x != 0) return;
-  const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
-                   (size_t)blockIdx.y * a.dst_seg_stride};
-  const int ndst = sv.ndst();
-  const char* src = static_cast<const char*>(sv.src(0, EB));
-  const size_t bytes = a.n * (size_t)EB;  // multiple of 16 (host-checked)
-  const size_t ntiles = (bytes + kBulkTile - 1) / kBulkTile;
-  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
-  const size_t mine = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  for (int s = 0; s < kBulkStages; ++s)
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[s])) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-
-  auto tile_bytes = [&](size_t t) -> uint32_t {
-    const size_t off = t * (size_t)kBulkTile;
-    const size_t left = bytes - off;
-    return (uint32_t)(left < (size_t)kBulkTile ? left : (size_t)kBulkTile);
-  };
-  auto issue_load = [&](size_t j) {  // j-th tile of this CTA into stage j % S
-    const size_t t = blockIdx.x + j * gridDim.x;
-    const int s = (int)(j % kBulkStages);
-    const uint32_t nb = tile_bytes(t);
-    const uint32_t bar = smem_u32(&bars[s]);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(nb)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(smem + (size_t)s * kBulkTile)),
-        "l"(src + t * (size_t)kBulkTile), "r"(nb), "r"(bar)
-        : "memory");
-  };
-
-  const size_t prologue = mine < (size_t)kBulkStages ? mine : (size_t)kBulkStages;
-  for (size_t j = 0; j < prologue; ++j) issue_load(j);
-  bool timed_out = false;
-  for (size_t j = 0; j < mine; ++j) {
-    const int s = (int)(j % kBulkStages);
-    const uint32_t parity = (uint32_t)((j / kBulkStages) & 1);
-    const uint32_t bar = smem_u32(&bars[s]);
-    uint32_t spins = 0;
-    while (!mbar_try_wait(bar, parity)) {
-      if (++spins >= kBulkSpinLimit) {
-        timed_out = true;
-        break;
-      }
-    }
-    if (timed_out) break;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    const size_t t = blockIdx.x + j * gridDim.x;
-    const uint32_t nb = tile_bytes(t);
-    const uint32_t from = smem_u32(smem + (size_t)s * kBulkTile);
-    for (int d = 0; d < ndst; ++d) {
-      char* dst = static_cast<char*>(sv.dst(d, EB)) + t * (size_t)kBulkTile;
-      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                   "r"(from), "r"(nb)
-                   : "memory");
-    }
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    if (j + kBulkStages < mine) {
-      // the stage is refilled only after its stores have read it
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      issue_load(j + kBulkStages);
-    }
-  }
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  if (timed_out) {
-    atomicExch(&g_bulk_timeout, 1u);
-    // let every load still in flight land before the CTA's shared memory goes
-    for (size_t j = 0; j < mine && j < (size_t)kBulkStages; ++j) {
-      const uint32_t bar = smem_u32(&bars[j % kBulkStages]);
-      for (uint32_t spins = 0; spins < kBulkSpinLimit; ++spins)
-        if (mbar_try_wait(bar, 0) || mbar_try_wait(bar, 1)) break;
-    }
-  }
-}
-
-template <int EB>
-cudaError_t launch_bulk_copy(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  const size_t smem = (size_t)kBulkStages * kBulkTile;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(bulk_copy_kernel<EB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const size_t ntiles = (a.n * (size_t)EB + kBulkTile - 1) / kBulkTile;
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bulk_copy_kernel<EB>, 32, smem);
-  if (per_sm < 1) per_sm = 1;
-  size_t cap = (size_t)per_sm * sm_count() / (size_t)nseg;
-  if (cap < 1) cap = 1;
-  const unsigned gx = (unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap);
-  return launch_kernel(bulk_copy_kernel<EB>, dim3(gx, (unsigned)nseg), dim3(32), smem, stream, a);
-}
-
-// Reads and clears this translation unit's bulk-copy timeout flag.
-inline cudaError_t bulk_copy_timeouts(uint32_t* out) {
-  uint32_t zero = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_bulk_timeout, sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_bulk_timeout, &zero, sizeof(uint32_t));
-  return e;
-}
-
 // Widest vector the addresses allow (RCC_VEC_BYTES=16 caps it at 16 bytes).
 inline int vec_cap() {
   static int cap = [] {
@@ -843,22 +697,6 @@ cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
 }
 
-template <typename T, int RED, bool FAST>
-cudaError_t launch_red(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  const int ns = a.src_per_seg ? 1 : a.nsrc;
-  switch (ns) {
-    case 1: return launch_ns<T, 1, RED, false>(nseg, a, stream);
-    case 2: return launch_ns<T, 2, RED, false>(nseg, a, stream);
-    case 3: return launch_ns<T, 3, RED, false>(nseg, a, stream);
-    case 4: return launch_ns<T, 4, RED, FAST>(nseg, a, stream);
-    case 5: return launch_ns<T, 5, RED, FAST>(nseg, a, stream);
-    case 6: return launch_ns<T, 6, RED, FAST>(nseg, a, stream);
-    case 7: return launch_ns<T, 7, RED, FAST>(nseg, a, stream);
-    case 8: return launch_ns<T, 8, RED, FAST>(nseg, a, stream);
-    default: return launch_ns<T, 0, RED, false>(nseg, a, stream);
-  }
-}
-
 // grid for the staged kernels: one CTA per tile up to RCC_WAVES waves
 template <typename KernelFn>
 unsigned staged_grid(KernelFn fn, size_t n, size_t tile, int nseg) {
@@ -887,21 +725,6 @@ cudaError_t launch_staged_reduce_ns(int nseg, const MultiPtrArgs& a, cudaStream_
   return launch_staged_reduce_w<T, NS, RED, FAST, 4>(nseg, a, stream);
 }
 
-template <typename T, int RED, bool FAST>
-cudaError_t launch_staged_reduce_red(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  switch (a.nsrc) {
-    case 1: return launch_staged_reduce_ns<T, 1, RED, false>(nseg, a, stream);
-    case 2: return launch_staged_reduce_ns<T, 2, RED, false>(nseg, a, stream);
-    case 3: return launch_staged_reduce_ns<T, 3, RED, false>(nseg, a, stream);
-    case 4: return launch_staged_reduce_ns<T, 4, RED, FAST>(nseg, a, stream);
-    case 5: return launch_staged_reduce_ns<T, 5, RED, FAST>(nseg, a, stream);
-    case 6: return launch_staged_reduce_ns<T, 6, RED, FAST>(nseg, a, stream);
-    case 7: return launch_staged_reduce_ns<T, 7, RED, FAST>(nseg, a, stream);
-    case 8: return launch_staged_reduce_ns<T, 8, RED, FAST>(nseg, a, stream);
-    default: return launch_staged_reduce_ns<T, 0, RED, false>(nseg, a, stream);
-  }
-}
-
 template <typename T>
 cudaError_t launch_staged_copy(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   if (a.vec_ok >= 32 && vec_cap() >= 32) {
@@ -916,35 +739,75 @@ cudaError_t launch_staged_copy(int nseg, const MultiPtrArgs& a, cudaStream_t str
                        0, stream, a);
 }
 
-template <typename T>
-cudaError_t launch_typed(Red red, bool fast, int nseg, const MultiPtrArgs& a,
-                         cudaStream_t stream) {
-  if (a.stage == kStageSources) {
-    switch (red) {
-      case kRedSum:
-        return fast ? launch_staged_reduce_red<T, kRedSum, true>(nseg, a, stream)
-                    : launch_staged_reduce_red<T, kRedSum, false>(nseg, a, stream);
-      case kRedMax: return launch_staged_reduce_red<T, kRedMax, false>(nseg, a, stream);
-      case kRedMin: return launch_staged_reduce_red<T, kRedMin, false>(nseg, a, stream);
+// ---- one reduction of one element type: the unit each build object holds --------
+// DT 0 = fp32, 1 = bf16.  FAST (pairwise-tree sums) covers 4..8 sources only;
+// the dispatcher sends every other source count to the rank-order unit, where
+// the tree and the fold are the same sum (1..3 sources) or the fold is the
+// defined order (runtime count).
+template <int DT>
+struct ElemOf {
+  using type = float;
+};
+template <>
+struct ElemOf<1> {
+  using type = __nv_bfloat16;
+};
+
+template <int DT, int RED, bool FAST>
+cudaError_t launch_part(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+  using T = typename ElemOf<DT>::type;
+  if constexpr (RED == kRedCopy) {
+    if (a.stage == kStageDestinations) return launch_staged_copy<T>(nseg, a, stream);
+    if (a.stage != kStageNone) return cudaErrorInvalidValue;
+    return launch_ns<T, 1, kRedCopy, false>(nseg, a, stream);
+  } else if constexpr (FAST) {
+    static_assert(RED == kRedSum, "only sums have a tree order");
+    if (a.stage == kStageSources) {
+      switch (a.nsrc) {
+        case 4: return launch_staged_reduce_ns<T, 4, RED, true>(nseg, a, stream);
+        case 5: return launch_staged_reduce_ns<T, 5, RED, true>(nseg, a, stream);
+        case 6: return launch_staged_reduce_ns<T, 6, RED, true>(nseg, a, stream);
+        case 7: return launch_staged_reduce_ns<T, 7, RED, true>(nseg, a, stream);
+        case 8: return launch_staged_reduce_ns<T, 8, RED, true>(nseg, a, stream);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    if (a.stage != kStageNone || a.src_per_seg) return cudaErrorInvalidValue;
+    switch (a.nsrc) {
+      case 4: return launch_ns<T, 4, RED, true>(nseg, a, stream);
+      case 5: return launch_ns<T, 5, RED, true>(nseg, a, stream);
+      case 6: return launch_ns<T, 6, RED, true>(nseg, a, stream);
+      case 7: return launch_ns<T, 7, RED, true>(nseg, a, stream);
+      case 8: return launch_ns<T, 8, RED, true>(nseg, a, stream);
       default: return cudaErrorInvalidValue;
     }
+  } else {
+    if (a.stage == kStageSources) {
+      switch (a.nsrc) {
+        case 1: return launch_staged_reduce_ns<T, 1, RED, false>(nseg, a, stream);
+        case 2: return launch_staged_reduce_ns<T, 2, RED, false>(nseg, a, stream);
+        case 3: return launch_staged_reduce_ns<T, 3, RED, false>(nseg, a, stream);
+        case 4: return launch_staged_reduce_ns<T, 4, RED, false>(nseg, a, stream);
+        case 5: return launch_staged_reduce_ns<T, 5, RED, false>(nseg, a, stream);
+        case 6: return launch_staged_reduce_ns<T, 6, RED, false>(nseg, a, stream);
+        case 7: return launch_staged_reduce_ns<T, 7, RED, false>(nseg, a, stream);
+        case 8: return launch_staged_reduce_ns<T, 8, RED, false>(nseg, a, stream);
+        default: return launch_staged_reduce_ns<T, 0, RED, false>(nseg, a, stream);
+      }
+    }
+    if (a.stage != kStageNone || a.src_per_seg) return cudaErrorInvalidValue;
+    switch (a.nsrc) {
+      case 1: return launch_ns<T, 1, RED, false>(nseg, a, stream);
+      case 2: return launch_ns<T, 2, RED, false>(nseg, a, stream);
+      case 3: return launch_ns<T, 3, RED, false>(nseg, a, stream);
+      case 4: return launch_ns<T, 4, RED, false>(nseg, a, stream);
+      case 5: return launch_ns<T, 5, RED, false>(nseg, a, stream);
+      case 6: return launch_ns<T, 6, RED, false>(nseg, a, stream);
+      case 7: return launch_ns<T, 7, RED, false>(nseg, a, stream);
+      case 8: return launch_ns<T, 8, RED, false>(nseg, a, stream);
+      default: return launch_ns<T, 0, RED, false>(nseg, a, stream);
+    }
   }
-  if (a.stage == kStageDestinations) {
-    if (red != kRedCopy) return cudaErrorInvalidValue;
-    return launch_staged_copy<T>(nseg, a, stream);
-  }
-  switch (red) {
-    case kRedSum:
-      return fast ? launch_red<T, kRedSum, true>(nseg, a, stream)
-                  : launch_red<T, kRedSum, false>(nseg, a, stream);
-    case kRedMax: return launch_red<T, kRedMax, false>(nseg, a, stream);
-    case kRedMin: return launch_red<T, kRedMin, false>(nseg, a, stream);
-    case kRedCopy:
-      if (RCC_BULK_COPY && a.vec_ok >= 16 && (a.n * Elem<T>::kBytes) % 16 == 0)
-        return launch_bulk_copy<Elem<T>::kBytes>(nseg, a, stream);
-      return launch_ns<T, 1, kRedCopy, false>(nseg, a, stream);
-  }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace mp

@@ -22,6 +22,7 @@
 //                     device-decision flows)
 //   gs_update_kernel  one launch per tensor: clip, decoupled decay, moments,
 //                     bias-corrected step on every optimizer-state replica
+//                     (32-byte accesses when every pointer allows)
 //   gs_update_multi_kernel  the same update for every tensor in one launch
 //                     (a comparison flow)
 //
@@ -47,11 +48,6 @@ __device__ __forceinline__ uint4 ld_vec(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-// Plain (write-back) 16-byte load for state that this kernel also writes.
-__device__ __forceinline__ float4 ld_state(const float* p) {
-  return *reinterpret_cast<const float4*>(p);
 }
 
 __device__ __forceinline__ void st_vec(void* p, const uint4& v) {
@@ -125,12 +121,18 @@ struct SqAcc {
   }
 };
 
-__device__ __forceinline__ void block_reduce_row(double s, uint32_t c, uint32_t* row) {
+// Block-wide sums of s (fp64) and c, written as one 12-byte row.  The count
+// is summed in 64 bits and stored saturated at 2^32 - 1: a combine level adds
+// up to 1024 rows of up to 2^24 elements each, and a wrapped count could read
+// as zero and let a step with non-finite gradients through.
+__device__ __forceinline__ void block_reduce_row(double s, uint64_t c, uint32_t* row) {
   __shared__ double ws[kWarps];
-  __shared__ uint32_t wc[kWarps];
+  __shared__ unsigned long long wc[kWarps];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, off);
-  c = __reduce_add_sync(0xFFFFFFFFu, c);
+  for (int off = 16; off > 0; off >>= 1) {
+    s += __shfl_down_sync(0xFFFFFFFFu, s, off);
+    c += __shfl_down_sync(0xFFFFFFFFu, (unsigned long long)c, off);
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
     ws[warp] = s;
@@ -139,15 +141,17 @@ __device__ __forceinline__ void block_reduce_row(double s, uint32_t c, uint32_t*
   __syncthreads();
   if (warp == 0) {
     s = lane < kWarps ? ws[lane] : 0.0;
-    c = lane < kWarps ? wc[lane] : 0u;
+    c = lane < kWarps ? wc[lane] : 0ull;
 #pragma unroll
-    for (int off = kWarps / 2; off > 0; off >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, off);
-    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    for (int off = kWarps / 2; off > 0; off >>= 1) {
+      s += __shfl_down_sync(0xFFFFFFFFu, s, off);
+      c += __shfl_down_sync(0xFFFFFFFFu, (unsigned long long)c, off);
+    }
     if (lane == 0) {
       const unsigned long long u = (unsigned long long)__double_as_longlong(s);
       row[0] = (uint32_t)(u & 0xFFFFFFFFull);
       row[1] = (uint32_t)(u >> 32);
-      row[2] = c;
+      row[2] = c > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)c;
     }
   }
 }
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kThreads)
   pdl_wait_then_release();
   const uint64_t r0 = (uint64_t)blockIdx.x * kFanIn;
   double s = 0.0;
-  uint32_t c = 0;
+  uint64_t c = 0;
 #pragma unroll
   for (int k = 0; k < kFanIn / kThreads; ++k) {
     const uint64_t r = r0 + threadIdx.x + (uint64_t)k * kThreads;
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(kThreads)
                      uint32_t* __restrict__ host_copy) {
   pdl_wait_then_release();
   double s = 0.0;
-  uint32_t c = 0;
+  uint64_t c = 0;
   for (uint64_t r = threadIdx.x; r < nrows; r += kThreads) {
     s += row_sum(in + r * 3);
     c += in[r * 3 + 2];
@@ -361,67 +365,120 @@ __device__ __forceinline__ StepView step_view(float clip, const AdamWScalars& s,
   return v;
 }
 
-// Elements [4v, 4v+4) of one tensor.  Returns false (having written nothing)
-// when the step is skipped.
-template <int REP>
-__device__ __forceinline__ bool update_vec4(float* const* P, int rep, const float* mean_grad,
-                                            const float* const* grads, int R, uint64_t v,
-                                            const StepView& sv) {
-  constexpr int RB = REP > 0 ? REP : 4;  // replicas per batch of loads
-  // the gradient inputs and the first batch of state, all in flight together
-  float4 g4;
-  if (mean_grad) {
-    const uint4 x = ld_vec(mean_grad + v * 4);
-    g4 = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
-                     __uint_as_float(x.w));
+// W consecutive floats: W = 4 (16-byte accesses) or W = 8 (32-byte accesses,
+// used when every pointer of the tensor is 32-byte aligned).
+template <int W>
+struct FVec {
+  float f[W];
+};
+
+// The mean gradient: read-only for the update kernel, read once.
+template <int W>
+__device__ __forceinline__ FVec<W> ld_grad(const float* p) {
+  FVec<W> v;
+  if constexpr (W == 4) {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.f[0]), "=f"(v.f[1]), "=f"(v.f[2]), "=f"(v.f[3])
+                 : "l"(p));
   } else {
-    g4 = *reinterpret_cast<const float4*>(grads[0] + v * 4);
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(v.f[0]), "=f"(v.f[1]), "=f"(v.f[2]), "=f"(v.f[3]), "=f"(v.f[4]),
+                   "=f"(v.f[5]), "=f"(v.f[6]), "=f"(v.f[7])
+                 : "l"(p));
+  }
+  return v;
+}
+
+// Scaled gradients and optimizer state: coherent loads (the state is written
+// back by the same thread), no L1 allocation.
+template <int W>
+__device__ __forceinline__ FVec<W> ld_rw(const float* p) {
+  FVec<W> v;
+  if constexpr (W == 4) {
+    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.f[0]), "=f"(v.f[1]), "=f"(v.f[2]), "=f"(v.f[3])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(v.f[0]), "=f"(v.f[1]), "=f"(v.f[2]), "=f"(v.f[3]), "=f"(v.f[4]),
+                   "=f"(v.f[5]), "=f"(v.f[6]), "=f"(v.f[7])
+                 : "l"(p));
+  }
+  return v;
+}
+
+template <int W>
+__device__ __forceinline__ void st_rw(float* p, const FVec<W>& v) {
+  if constexpr (W == 4) {
+    asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.f[0]), "f"(v.f[1]),
+                 "f"(v.f[2]), "f"(v.f[3])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v.f[0]),
+                 "f"(v.f[1]), "f"(v.f[2]), "f"(v.f[3]), "f"(v.f[4]), "f"(v.f[5]), "f"(v.f[6]),
+                 "f"(v.f[7])
+                 : "memory");
+  }
+}
+
+// Elements [W*v, W*v + W) of one tensor.  Returns false (having written
+// nothing) when the step is skipped.  The gradient and the first batch of
+// state replicas are all loaded before any arithmetic; replicas beyond the
+// batch (RB: 4 with 16-byte vectors; 1 with 32-byte ones, which keeps the
+// kernel near 60 registers and 4 CTAs per SM) follow batch by batch.
+template <int REP, int W>
+__device__ __forceinline__ bool update_vec(float* const* P, int rep, const float* mean_grad,
+                                           const float* const* grads, int R, uint64_t v,
+                                           const StepView& sv) {
+  constexpr int RBMAX = W == 8 ? 1 : 4;
+  constexpr int RB = REP > 0 && REP < RBMAX ? REP : RBMAX;  // replicas per batch of loads
+  const uint64_t off = v * W;
+  FVec<W> g;
+  if (mean_grad) {
+    g = ld_grad<W>(mean_grad + off);
+  } else {
+    g = ld_rw<W>(grads[0] + off);
     for (int q = 1; q < R; ++q) {
-      const float4 y = *reinterpret_cast<const float4*>(grads[q] + v * 4);
-      g4.x = __fadd_rn(g4.x, y.x);
-      g4.y = __fadd_rn(g4.y, y.y);
-      g4.z = __fadd_rn(g4.z, y.z);
-      g4.w = __fadd_rn(g4.w, y.w);
+      const FVec<W> y = ld_rw<W>(grads[q] + off);
+#pragma unroll
+      for (int e = 0; e < W; ++e) g.f[e] = __fadd_rn(g.f[e], y.f[e]);
     }
   }
-  float4 p[RB], m[RB], w[RB];
+  FVec<W> p[RB], m[RB], w[RB];
 #pragma unroll
   for (int k = 0; k < RB; ++k) {
     if (k < rep) {
-      p[k] = ld_state(P[k] + v * 4);
-      m[k] = ld_state(P[rep + k] + v * 4);
-      w[k] = ld_state(P[2 * rep + k] + v * 4);
+      p[k] = ld_rw<W>(P[k] + off);
+      m[k] = ld_rw<W>(P[rep + k] + off);
+      w[k] = ld_rw<W>(P[2 * rep + k] + off);
     }
   }
   if (sv.d.skip) return false;  // skipped step: state untouched
-  float gv[4] = {g4.x, g4.y, g4.z, g4.w};
   if (!mean_grad) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(div_by_ranks(gv[e], R), sv.inv_scale);
+    for (int e = 0; e < W; ++e) g.f[e] = __fmul_rn(div_by_ranks(g.f[e], R), sv.inv_scale);
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], sv.d.coef);
+  for (int e = 0; e < W; ++e) g.f[e] = __fmul_rn(g.f[e], sv.d.coef);
   for (int r0 = 0; r0 < rep; r0 += RB) {
     if (r0 > 0) {
 #pragma unroll
       for (int k = 0; k < RB; ++k) {
         if (r0 + k < rep) {
-          p[k] = ld_state(P[r0 + k] + v * 4);
-          m[k] = ld_state(P[rep + r0 + k] + v * 4);
-          w[k] = ld_state(P[2 * rep + r0 + k] + v * 4);
+          p[k] = ld_rw<W>(P[r0 + k] + off);
+          m[k] = ld_rw<W>(P[rep + r0 + k] + off);
+          w[k] = ld_rw<W>(P[2 * rep + r0 + k] + off);
         }
       }
     }
 #pragma unroll
     for (int k = 0; k < RB; ++k) {
       if (r0 + k < rep) {
-        adamw_elem(gv[0], sv.sc, p[k].x, m[k].x, w[k].x);
-        adamw_elem(gv[1], sv.sc, p[k].y, m[k].y, w[k].y);
-        adamw_elem(gv[2], sv.sc, p[k].z, m[k].z, w[k].z);
-        adamw_elem(gv[3], sv.sc, p[k].w, m[k].w, w[k].w);
-        *reinterpret_cast<float4*>(P[r0 + k] + v * 4) = p[k];
-        *reinterpret_cast<float4*>(P[rep + r0 + k] + v * 4) = m[k];
-        *reinterpret_cast<float4*>(P[2 * rep + r0 + k] + v * 4) = w[k];
+#pragma unroll
+        for (int e = 0; e < W; ++e) adamw_elem(g.f[e], sv.sc, p[k].f[e], m[k].f[e], w[k].f[e]);
+        st_rw<W>(P[r0 + k] + off, p[k]);
+        st_rw<W>(P[rep + r0 + k] + off, m[k]);
+        st_rw<W>(P[2 * rep + r0 + k] + off, w[k]);
       }
     }
   }
@@ -451,8 +508,10 @@ __device__ __forceinline__ void update_one(float* const* P, int rep, const float
   }
 }
 
-// One launch per tensor (the pages' design).
-template <int REP>  // REP > 0: compile-time replica count; 0: runtime
+// One launch per tensor (the pages' design).  W: floats per vector (8 when
+// the host found every pointer of the tensor 32-byte aligned, else 4; a.vec_ok
+// 0 means scalars only).
+template <int REP, int W>  // REP > 0: compile-time replica count; 0: runtime
 __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_constant__ GsUpdateArgs a) {
   // The next kernel is released only once this CTA's vectors are done: these
   // kernels run on parallel chains, and CTAs released early would sit in SM
@@ -460,14 +519,14 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
   pdl_wait();
   const int rep = REP > 0 ? REP : a.replicas;
   const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
-  const uint64_t nv = a.vec_ok ? a.numel / 4 : 0;
+  const uint64_t nv = a.vec_ok ? a.numel / W : 0;
   const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
   const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
   for (uint64_t v = tid; v < nv; v += nthreads)
-    if (!update_vec4<REP>(a.state, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
+    if (!update_vec<REP, W>(a.state, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
   pdl_release();
   if (sv.d.skip) return;
-  for (uint64_t i = nv * 4 + tid; i < a.numel; i += nthreads)
+  for (uint64_t i = nv * W + tid; i < a.numel; i += nthreads)
     update_one(a.state, rep, a.mean_grad, a.grads, a.R, i, sv);
 }
 
@@ -499,7 +558,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t v1 = c1 / 4;
     scalar_from = v1 * 4;
     for (uint64_t v = c0 / 4 + threadIdx.x; v < v1; v += kThreads)
-      if (!update_vec4<REP>(P, rep, t.mean_grad, g, a.R, v, sv)) return;
+      if (!update_vec<REP, 4>(P, rep, t.mean_grad, g, a.R, v, sv)) return;
   }
   if (sv.d.skip) return;
   for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads)
@@ -605,8 +664,9 @@ cudaError_t launch_gs_decide(const uint32_t* report, double max_grad_norm, GsDec
                        out);
 }
 
-cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
-  const uint64_t units = a.vec_ok ? (a.numel + 3) / 4 : a.numel;
+template <int W>
+cudaError_t launch_gs_update_w(const GsUpdateArgs& a, cudaStream_t stream) {
+  const uint64_t units = a.vec_ok ? (a.numel + W - 1) / W : a.numel;
   uint64_t blocks = (units + kThreads - 1) / kThreads;
   // one vector per thread up to 64 CTAs per SM, grid-stride beyond
   const uint64_t cap = (uint64_t)gs::sm_count() * 64;
@@ -614,12 +674,16 @@ cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
   if (blocks < 1) blocks = 1;
   const dim3 grid((unsigned)blocks), block(kThreads);
   switch (a.replicas) {
-    case 1: return launch_kernel(gs::gs_update_kernel<1>, grid, block, 0, stream, a);
-    case 2: return launch_kernel(gs::gs_update_kernel<2>, grid, block, 0, stream, a);
-    case 4: return launch_kernel(gs::gs_update_kernel<4>, grid, block, 0, stream, a);
-    case 8: return launch_kernel(gs::gs_update_kernel<8>, grid, block, 0, stream, a);
-    default: return launch_kernel(gs::gs_update_kernel<0>, grid, block, 0, stream, a);
+    case 1: return launch_kernel(gs::gs_update_kernel<1, W>, grid, block, 0, stream, a);
+    case 2: return launch_kernel(gs::gs_update_kernel<2, W>, grid, block, 0, stream, a);
+    case 4: return launch_kernel(gs::gs_update_kernel<4, W>, grid, block, 0, stream, a);
+    case 8: return launch_kernel(gs::gs_update_kernel<8, W>, grid, block, 0, stream, a);
+    default: return launch_kernel(gs::gs_update_kernel<0, W>, grid, block, 0, stream, a);
   }
+}
+
+cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream) {
+  return a.vec_ok == 32 ? launch_gs_update_w<8>(a, stream) : launch_gs_update_w<4>(a, stream);
 }
 
 // ---- statistics without allocation -----------------------------------------

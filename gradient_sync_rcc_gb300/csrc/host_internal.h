@@ -144,6 +144,10 @@ struct Scratch {
   cudaStream_t branch[kMaxBranches] = {};
   cudaEvent_t fork_ev = nullptr;
   cudaEvent_t join_ev[kMaxBranches] = {};
+  // RCC_STEP_TIMING: events around the phases of the last grad-sync call
+  static constexpr int kTimeEvents = 5;
+  cudaEvent_t time_ev[kTimeEvents] = {};
+  bool timed = false;               // the last call recorded all of them
   cudaGraphExec_t graph_exec = nullptr;
   uint64_t graph_gen = 0;           // desc_gen the graph was captured for
   size_t graph_P = 0;
@@ -225,6 +229,8 @@ inline void free_scratch(Scratch& s) {
     if (s.join_ev[k]) cudaEventDestroy(s.join_ev[k]);
   }
   if (s.fork_ev) cudaEventDestroy(s.fork_ev);
+  for (int k = 0; k < Scratch::kTimeEvents; ++k)
+    if (s.time_ev[k]) cudaEventDestroy(s.time_ev[k]);
   s = Scratch{};
 }
 
@@ -273,6 +279,7 @@ inline rcc_status missing_session() {
 
 inline size_t elem_bytes(rcc_dtype t) { return t == RCC_F32 ? 4 : 2; }
 inline bool valid_op(int op) { return op >= RCC_SUM && op <= RCC_MIN; }
+constexpr unsigned kSessionFlags = RCC_DETERMINISTIC | RCC_STEP_TIMING;
 
 inline bool overlap(const void* a, size_t an, const void* b, size_t bn) {
   if (an == 0 || bn == 0) return false;
@@ -362,6 +369,31 @@ inline rcc::Red red_of(rcc_op op) {
   }
 }
 
+// Picks the build object of the pass: the pairwise tree applies to sums over
+// 4..8 sources (with fewer the tree is the rank-order fold; a runtime rank
+// count folds in rank order).
+template <int DT>
+inline cudaError_t launch_multi_ptr_t(rcc::Red red, bool fast, int nseg, const MultiPtrArgs& a,
+                                      cudaStream_t st) {
+  using rcc::mp::launch_part;
+  switch (red) {
+    case rcc::kRedSum:
+      if (fast && !a.src_per_seg && a.nsrc >= 4 && a.nsrc <= 8)
+        return launch_part<DT, rcc::kRedSum, true>(nseg, a, st);
+      return launch_part<DT, rcc::kRedSum, false>(nseg, a, st);
+    case rcc::kRedMax: return launch_part<DT, rcc::kRedMax, false>(nseg, a, st);
+    case rcc::kRedMin: return launch_part<DT, rcc::kRedMin, false>(nseg, a, st);
+    case rcc::kRedCopy: return launch_part<DT, rcc::kRedCopy, false>(nseg, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+inline cudaError_t launch_multi_ptr(int dt, rcc::Red red, bool fast, int nseg,
+                                    const MultiPtrArgs& a, cudaStream_t st) {
+  return dt == 0 ? launch_multi_ptr_t<0>(red, fast, nseg, a, st)
+                 : launch_multi_ptr_t<1>(red, fast, nseg, a, st);
+}
+
 inline rcc_status launch(const Session& s, rcc::Red red, int nseg, const MultiPtrArgs& a,
                   rcc_stream_t stream, ArrivalSync* sync = nullptr) {
   const bool fast = (s.flags.load() & RCC_DETERMINISTIC) == 0;
@@ -381,8 +413,7 @@ inline rcc_status launch(const Session& s, rcc::Red red, int nseg, const MultiPt
       if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
     }
   }
-  cudaError_t e = s.dtype == RCC_F32 ? rcc::launch_multi_ptr_f32(red, fast, nseg, a, st)
-                                     : rcc::launch_multi_ptr_bf16(red, fast, nseg, a, st);
+  cudaError_t e = launch_multi_ptr(s.dtype == RCC_F32 ? 0 : 1, red, fast, nseg, a, st);
   if (e != cudaSuccess) return cuda_fail(e, "collective kernel launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (sync) {

@@ -220,6 +220,15 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     sc.stale = false;
   }
   if ((st = ensure_fixed_scratch(sc)) != RCC_OK) return st;
+  const bool timing = (s->flags.load() & RCC_STEP_TIMING) != 0;
+  sc.timed = false;
+  if (timing) {
+    for (int k = 0; k < Scratch::kTimeEvents; ++k) {
+      if (sc.time_ev[k]) continue;
+      cudaError_t te = cudaEventCreate(&sc.time_ev[k]);
+      if (te != cudaSuccess) return cuda_fail(te, "cudaEventCreate(timing)");
+    }
+  }
   if ((st = ensure_dev(&sc.rows, &sc.rows_cap, (size_t)total_rows * 12, "cudaMalloc(rows)")) !=
       RCC_OK)
     return st;
@@ -258,19 +267,26 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     const rcc_param_set& ps = params[p];
     bool gv = ps.mean_grad == nullptr || aligned16(ps.mean_grad);
     bool gv32 = rows8 && (ps.mean_grad == nullptr || aligned32(ps.mean_grad));
+    bool grads32 = true;
     for (int r = 0; r < R; ++r) {
       gtab[p * R + r] = ps.grads[r];
       gv = gv && aligned16(ps.grads[r]);
-      gv32 = gv32 && aligned32(ps.grads[r]);
+      grads32 = grads32 && aligned32(ps.grads[r]);
     }
+    gv32 = gv32 && grads32;
     bool uv = gv;
+    // 32-byte update vectors: the gradient the update reads (the mean
+    // gradient, else every rank's) and every state pointer 32-byte aligned
+    bool uv32 = wide_ok && (ps.mean_grad ? aligned32(ps.mean_grad) : grads32);
     for (int k = 0; k < rep; ++k) {
       stab[p * 3 * rep + k] = ps.params[k];
       stab[p * 3 * rep + rep + k] = ps.exp_avg[k];
       stab[p * 3 * rep + 2 * rep + k] = ps.exp_avg_sq[k];
       uv = uv && aligned16(ps.params[k]) && aligned16(ps.exp_avg[k]) && aligned16(ps.exp_avg_sq[k]);
+      uv32 = uv32 && aligned32(ps.params[k]) && aligned32(ps.exp_avg[k]) &&
+             aligned32(ps.exp_avg_sq[k]);
     }
-    upd_vec[p] = uv ? 1 : 0;
+    upd_vec[p] = uv32 && uv ? 32 : (uv ? 16 : 0);
     rcc::GsTensor t{};
     t.numel = ps.numel;
     t.row_begin = row;
@@ -354,8 +370,14 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   ga.elems_per_row = epr;
   ga.R = R;
   ga.inv_scale = inv_scale;
+  // RCC_STEP_TIMING: an event at each phase boundary on the call's stream
+  auto mark = [&](int k) -> cudaError_t {
+    return timing ? cudaEventRecord(sc.time_ev[k], cs) : cudaSuccess;
+  };
+  if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
   if ((e = rcc::launch_gs_stats(ga, cs)) != cudaSuccess) return cuda_fail(e, "statistics kernel");
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
 
   const uint32_t* src = static_cast<const uint32_t*>(sc.rows);
   uint64_t rows = total_rows;
@@ -385,6 +407,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
           cudaSuccess)
     return cuda_fail(e, "report readback");
   if ((e = cudaEventRecord(sc.report_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
 
   // One update kernel per tensor, spread over parallel chains forked from
   // (and joined back into) `origin`: largest tensors first onto the least
@@ -532,6 +555,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     ua.clip_coef = 1.0f;
     ua.decision = sc.decision_dev;
     ua.dev_scalars = sc.scalars_dev;
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
     if (cfg->flags & RCC_ADAMW_GRAPH) {
       if ((st = replay_graph()) != RCC_OK) return st;
     } else {
@@ -574,6 +598,10 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   rep_out.combine_region_bytes = region_bytes;
 
   rep_out.update_launches = device_updates;
+  rep_out.report_words[0] = sc.report_host[0];
+  rep_out.report_words[1] = sc.report_host[1];
+  rep_out.report_words[2] = sc.report_host[2];
+  if (!on_device && (e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
   if (skip) {
     state->scale *= state->backoff_factor;
     state->growth_tracker = 0;
@@ -609,9 +637,34 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       state->growth_tracker = 0;
     }
   }
+  if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
   if ((e = cudaEventRecord(sc.done_ev, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   sc.done_recorded = true;
+  sc.timed = timing;
   if (report) *report = rep_out;
+  return RCC_OK;
+}
+
+rcc_status rcc_last_step_times(rcc_comm comm, float out_ms[4]) {
+  t_err.clear();
+  if (!out_ms) return fail(RCC_ERR_INVALID_ARGUMENT, "out_ms is NULL");
+  auto s = lookup(comm);
+  if (!s) return missing_session();
+  std::lock_guard<std::mutex> lock(s->mu);
+  Scratch& sc = s->sc;
+  if (!sc.timed)
+    return fail(RCC_ERR_INVALID_ARGUMENT,
+                "no timed grad-sync call on this session (set RCC_STEP_TIMING first)");
+  rcc_status st = check_device(s->device);
+  if (st != RCC_OK) return st;
+  if ((st = wait_event(sc.time_ev[Scratch::kTimeEvents - 1], "timed grad-sync call")) != RCC_OK)
+    return st;
+  for (int k = 0; k + 1 < Scratch::kTimeEvents; ++k) {
+    float ms = 0.0f;
+    cudaError_t e = cudaEventElapsedTime(&ms, sc.time_ev[k], sc.time_ev[k + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    out_ms[k] = ms;
+  }
   return RCC_OK;
 }
 

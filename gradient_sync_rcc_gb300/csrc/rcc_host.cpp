@@ -61,8 +61,8 @@ rcc_status rcc_register(int device, int num_ranks, rcc_dtype dtype, unsigned fla
                 RCC_MAX_RANKS);
   if (dtype != RCC_F32 && dtype != RCC_BF16)
     return fail(RCC_ERR_INVALID_ARGUMENT, "dtype %d is not an rcc_dtype", (int)dtype);
-  if (flags & ~RCC_DETERMINISTIC)
-    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags & ~RCC_DETERMINISTIC);
+  if (flags & ~kSessionFlags)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags & ~kSessionFlags);
   std::lock_guard<std::mutex> lock(g_reg_mu);
   int free_slot = -1;
   for (int i = 0; i < kSlots; ++i) {
@@ -87,8 +87,8 @@ rcc_status rcc_set_flags(rcc_comm comm, unsigned flags) {
   t_err.clear();
   auto s = lookup(comm);
   if (!s) return missing_session();
-  if (flags & ~RCC_DETERMINISTIC)
-    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags & ~RCC_DETERMINISTIC);
+  if (flags & ~kSessionFlags)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags & ~kSessionFlags);
   s->flags.store(flags);
   return RCC_OK;
 }
@@ -116,11 +116,6 @@ rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream) {
   }
   unregister(comm);
   wake_waiters(*s);
-  // a bulk-copy CTA that gave up waiting leaves its flag raised
-  uint32_t f32 = 0, bf16 = 0;
-  if (rcc::bulk_copy_timeouts_f32(&f32) == cudaSuccess &&
-      rcc::bulk_copy_timeouts_bf16(&bf16) == cudaSuccess && (f32 | bf16))
-    return fail(RCC_ERR_TIMEOUT, "a bulk-copy wait gave up: some copy output is incomplete");
   return RCC_OK;
 }
 

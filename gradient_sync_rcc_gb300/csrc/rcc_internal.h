@@ -55,14 +55,14 @@ struct MultiPtrArgs {
 // destinations (copies: loads staged through shared memory, vector stores).
 enum Stage : int { kStageNone = 0, kStageSources = 1, kStageDestinations = 2 };
 
-// One launch of the pass; fast selects the pairwise-tree sum.
-cudaError_t launch_multi_ptr_f32(Red red, bool fast, int nseg, const MultiPtrArgs& a,
-                                 cudaStream_t stream);
-cudaError_t launch_multi_ptr_bf16(Red red, bool fast, int nseg, const MultiPtrArgs& a,
-                                  cudaStream_t stream);
-// Read and clear the flag a bulk-copy CTA raises when a bounded wait gave up.
-cudaError_t bulk_copy_timeouts_f32(uint32_t* out);
-cudaError_t bulk_copy_timeouts_bf16(uint32_t* out);
+// One launch of the pass for element type DT (0 fp32, 1 bf16) and reduction
+// RED; FAST (sums over 4..8 sources) selects the pairwise tree.  Each
+// combination the host names is instantiated in its own build object
+// (collectives_part.cu).
+namespace mp {
+template <int DT, int RED, bool FAST>
+cudaError_t launch_part(int nseg, const MultiPtrArgs& a, cudaStream_t stream);
+}  // namespace mp
 
 // ---- gradient sync -------------------------------------------------------
 
@@ -126,7 +126,8 @@ struct GsUpdateArgs {
   uint64_t numel;
   int R;
   int replicas;
-  int vec_ok;                   // every pointer 16-byte aligned
+  int vec_ok;                   // alignment class of every pointer of the tensor, in
+                                //   bytes: 32 (32-byte vectors), 16, or 0 (scalars)
   float inv_scale;
   float clip_coef;
   AdamWScalars s;

@@ -32,6 +32,7 @@ F32, BF16 = 0, 1
 SUM, MEAN, MAX, MIN = 0, 1, 2, 3
 OPS = {"sum": SUM, "mean": MEAN, "max": MAX, "min": MIN}
 DETERMINISTIC = 0x1
+STEP_TIMING = 0x2
 ADAMW_DEVICE_DECISION = 0x1
 ADAMW_GRAPH = 0x2
 ADAMW_MULTI_TENSOR = 0x4
@@ -44,7 +45,8 @@ SYMBOLS = ["rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_
            "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc", "rcc_last_error_message",
            "rcc_status_string", "rcc_kernel_launch_count", "rcc_all_reduce_rank",
            "rcc_reduce_rank", "rcc_broadcast_rank", "rcc_reduce_scatter_rank",
-           "rcc_all_gather_rank", "rcc_all_to_all_single", "rcc_all_gather_list"]
+           "rcc_all_gather_rank", "rcc_all_to_all_single", "rcc_all_gather_list",
+           "rcc_last_step_times"]
 
 
 class ParamSet(C.Structure):
@@ -72,7 +74,8 @@ class StepReport(C.Structure):
     _fields_ = [("sum_sq", C.c_double), ("grad_norm", C.c_double), ("scale_used", C.c_double),
                 ("nonfinite", C.c_uint32), ("skipped", C.c_int32), ("clip_coef", C.c_float),
                 ("combine_launches", C.c_int32), ("stats_rows", C.c_uint64),
-                ("combine_region_bytes", C.c_uint64), ("update_launches", C.c_uint64)]
+                ("combine_region_bytes", C.c_uint64), ("update_launches", C.c_uint64),
+                ("report_words", C.c_uint32 * 3)]
 
 
 _lib = None
@@ -113,11 +116,13 @@ def lib():
         L.rcc_all_gather_rank.argtypes = [vp, C.c_int, vp, vp, sz, vp]
         L.rcc_all_to_all_single.argtypes = [vp, _PP, _PP, C.POINTER(C.c_size_t), vp]
         L.rcc_all_gather_list.argtypes = [vp, _PP, _PP, C.POINTER(C.c_size_t), vp]
+        L.rcc_last_step_times.argtypes = [vp, C.POINTER(C.c_float)]
         for name in ("rcc_register", "rcc_set_flags", "rcc_finish", "rcc_reset", "rcc_all_reduce",
                      "rcc_reduce", "rcc_broadcast", "rcc_reduce_scatter", "rcc_all_gather",
                      "rcc_grad_sync_adamw", "rcc_grad_stats_noalloc", "rcc_all_reduce_rank",
                      "rcc_reduce_rank", "rcc_broadcast_rank", "rcc_reduce_scatter_rank",
-                     "rcc_all_gather_rank", "rcc_all_to_all_single", "rcc_all_gather_list"):
+                     "rcc_all_gather_rank", "rcc_all_to_all_single", "rcc_all_gather_list",
+                     "rcc_last_step_times"):
             getattr(L, name).restype = st
         L.rcc_last_error_message.restype = C.c_char_p
         L.rcc_last_error_message.argtypes = []
@@ -183,16 +188,29 @@ def _op(op):
 
 # ------------------------------------------------------------- sessions
 
-def register(device=0, num_ranks=4, dtype=F32, deterministic=True):
+def _flags(deterministic, step_timing):
+    return (DETERMINISTIC if deterministic else 0) | (STEP_TIMING if step_timing else 0)
+
+
+def register(device=0, num_ranks=4, dtype=F32, deterministic=True, step_timing=False):
     """rcc_register; returns the session handle (an int)."""
     h = C.c_void_p()
-    flags = DETERMINISTIC if deterministic else 0
-    _check(lib().rcc_register(device, num_ranks, dtype, flags, C.byref(h)))
+    _check(lib().rcc_register(device, num_ranks, dtype, _flags(deterministic, step_timing),
+                              C.byref(h)))
     return h.value
 
 
-def set_flags(comm, deterministic=True):
-    _check(lib().rcc_set_flags(comm, DETERMINISTIC if deterministic else 0))
+def set_flags(comm, deterministic=True, step_timing=False):
+    _check(lib().rcc_set_flags(comm, _flags(deterministic, step_timing)))
+
+
+def last_step_times(comm):
+    """rcc_last_step_times: ms of the last timed grad-sync call's phases
+    (statistics kernel, combines + report, report to first update launch,
+    updates)."""
+    out = (C.c_float * 4)()
+    _check(lib().rcc_last_step_times(comm, out))
+    return list(out)
 
 
 def finish(comm, stream=None):
@@ -333,9 +351,25 @@ def grad_sync_adamw(comm, param_sets, cfg, state, stream=None):
 
 def grad_stats_noalloc(grads, loss_scale, report, mean_grad=None, stream=None):
     """rcc_grad_stats_noalloc for one tensor: grads are R device tensors,
-    report a device tensor of at least 12 bytes (e.g. torch.int32 x 3)."""
+    report a device tensor of at least 12 bytes (e.g. torch.int32 x 3).
+
+    The C call receives bare pointers and one element count, so it cannot
+    see a short, strided or bf16 rank tensor; those are rejected here."""
+    import torch
+    if not grads:
+        raise ValueError("grads is empty")
+    n, dev = grads[0].numel(), grads[0].device
+    for t in list(grads) + ([mean_grad] if mean_grad is not None else []):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("gradients and mean_grad must be contiguous float32 tensors")
+        if t.numel() != n or t.device != dev:
+            raise ValueError("every gradient and mean_grad must have %d elements on %s" % (n, dev))
+    if report.device != dev or not report.is_contiguous() or \
+            report.numel() * report.element_size() < 12:
+        raise ValueError("report must be a contiguous device tensor of at least 12 bytes on %s"
+                         % dev)
     _check(lib().rcc_grad_stats_noalloc(ptr_array([g.data_ptr() for g in grads]), len(grads),
-                                        grads[0].numel(), float(loss_scale), _ptr(mean_grad),
+                                        n, float(loss_scale), _ptr(mean_grad),
                                         report.data_ptr(), _stream(stream)))
 
 

@@ -47,8 +47,6 @@
  *                      (1..32, default 16).
  *   RCC_AUTO_GRAPH=0   the default grad-sync flow never switches to graph
  *                      replay.
- * Built with -DRCC_BULK_COPY=1, the copy collectives go through shared
- * memory with bulk copies instead of vector loads (slower; a comparison).
  */
 #ifndef RCC_H
 #define RCC_H
@@ -96,6 +94,12 @@ typedef enum { RCC_SUM = 0, RCC_MEAN = 1, RCC_MAX = 2, RCC_MIN = 3 } rcc_op;
  * shorter dependency chain, results within the fp32 error bound).  MAX and
  * MIN are exact in both modes. */
 #define RCC_DETERMINISTIC 0x1u
+/* Session flag RCC_STEP_TIMING: rcc_grad_sync_adamw records CUDA events
+ * between its phases, which rcc_last_step_times reads back.  A diagnostic: the
+ * events sit between kernels that otherwise overlap their launches
+ * (programmatic dependent launch), so a timed step can run a few microseconds
+ * longer. */
+#define RCC_STEP_TIMING 0x2u
 
 /* Opaque session handle.  A finished or reset handle stays detectable: calls
  * on it return RCC_ERR_MISSING_REGISTRATION, never touch freed memory. */
@@ -301,6 +305,9 @@ typedef struct {
   uint64_t stats_rows;         /* rows written by the statistics kernel */
   uint64_t combine_region_bytes; /* bytes of the reused reduction region touched (<= 49,200) */
   uint64_t update_launches;    /* AdamW update kernels launched (num_params or 0) */
+  uint32_t report_words[3];    /* the 12-byte report as read back: low and high 32-bit
+                                  words of the fp64 sum of g^2, then the u32 count of
+                                  non-finite g (saturated at 2^32 - 1) */
 } rcc_step_report;
 
 /* [ruCCL §6 + RUDA-T].  One data-parallel optimizer step over num_params
@@ -334,6 +341,19 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params,
                                int num_params, const rcc_adamw_cfg* cfg,
                                rcc_optim_state* state, rcc_step_report* report,
                                rcc_stream_t stream);
+
+/* Phase times of the session's most recent rcc_grad_sync_adamw call, made
+ * while the session had RCC_STEP_TIMING set, in milliseconds of GPU time
+ * between CUDA events on the call's stream:
+ *   out_ms[0] statistics kernel (mean, unscale, one row per block);
+ *   out_ms[1] the fan-in-1024 combines and the 12-byte report;
+ *   out_ms[2] from the report to the first update launch: in the default
+ *             flow the readback, the host's decision and the launch issue;
+ *             in the device-decision flows the decision kernel;
+ *   out_ms[3] the update launches (0 launches on a skipped host-flow step).
+ * Waits (bounded) for the call's work.  RCC_ERR_INVALID_ARGUMENT when the
+ * session has no timed call. */
+rcc_status rcc_last_step_times(rcc_comm comm, float out_ms[4]);
 
 /* ---- gradient statistics without allocation ------------------------------- */
 

@@ -111,9 +111,19 @@ def test_null_and_forged_handles(L):
 
 def test_set_flags_validation(L, comm):
     a = comm()
-    assert L.raw("rcc_set_flags", a, 0x2) == L.ERR_INVALID_ARGUMENT
+    assert L.raw("rcc_set_flags", a, 0x4) == L.ERR_INVALID_ARGUMENT
     assert L.raw("rcc_set_flags", a, 0) == L.OK
     assert L.raw("rcc_set_flags", a, 1) == L.OK
+    assert L.raw("rcc_set_flags", a, L.DETERMINISTIC | L.STEP_TIMING) == L.OK
+
+
+def test_step_times_need_a_timed_call(L, comm):
+    a = comm()
+    out = (C.c_float * 4)()
+    assert L.raw("rcc_last_step_times", a, out) == L.ERR_INVALID_ARGUMENT
+    assert "RCC_STEP_TIMING" in L.last_error()
+    assert L.raw("rcc_last_step_times", a, None) == L.ERR_INVALID_ARGUMENT
+    assert L.raw("rcc_last_step_times", None, out) == L.ERR_MISSING_REGISTRATION
 
 
 # ---------------------------------------------------------------- all_reduce
