@@ -27,9 +27,8 @@
  *
  * Parity status: every function here is pinned by tests that do not call it
  * twice (closed forms, exact integer sums, correctly rounded sums, hand-derived
- * rounding cases, library bf16 conversion), except orc_report_pack (the
- * 12-byte report's internal layout, which the pages do not fix): parity
- * unpinned.
+ * rounding cases, library bf16 conversion, the byte layout of a packed
+ * fp64 + u32 record).
  */
 #ifndef RCC_ORACLE_H
 #define RCC_ORACLE_H
@@ -158,8 +157,10 @@ void orc_grad_sync_adamw_step(int R, int P, const size_t* numel,
                               int64_t* step, orc_scaler* scaler, orc_stats* st,
                               orc_decision* d);
 
-/* the 12-byte report: {fp64 sum of squares, u32 non-finite count} packed as
- * three little-endian u32 words (parity unpinned: the pages fix only the size) */
+/* the 12-byte report [RUDA-T: 12 bytes read back before the update; the page
+ * fixes only the size]: {fp64 sum of squares, u32 non-finite count} as three
+ * little-endian u32 words (low word of the sum, high word, count); a count
+ * beyond 2^32 - 1 is stored as 2^32 - 1 */
 void orc_report_pack(const orc_stats* st, uint32_t out[3]);
 
 #ifdef __cplusplus

@@ -71,6 +71,13 @@ MUTANTS = [
     ("step counted when skipped", "  if (d->skip) {\n    orc_scaler_update(scaler, 1);\n    return;",
      "  if (d->skip) {\n    orc_scaler_update(scaler, 1);\n    *step += 1;\n    return;",
      [pins.test_skip_on_nonfinite_and_scaler]),
+    ("report words swapped", "out[0] = (uint32_t)(u & 0xFFFFFFFFu);\n  out[1] = (uint32_t)(u >> 32);",
+     "out[0] = (uint32_t)(u >> 32);\n  out[1] = (uint32_t)(u & 0xFFFFFFFFu);",
+     [pins.test_report_pack_layout]),
+    ("report count wraps", "(uint32_t)(st->nonfinite > 0xFFFFFFFFull ? 0xFFFFFFFFu : st->nonfinite)",
+     "(uint32_t)st->nonfinite", [pins.test_report_pack_layout]),
+    ("report drops the compensation", "  double s = orc_stats_value(st);\n  uint64_t u;",
+     "  double s = st->sum;\n  uint64_t u;", [pins.test_report_pack_layout]),
 ]
 
 

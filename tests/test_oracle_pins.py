@@ -543,3 +543,28 @@ def test_full_step_matches_piecewise_closed_form(orc):
         gp = g * float(d.clip_coef)
         want = (1 - LR * WD) * q0.astype(np.float64) - LR * gp / (np.abs(gp) + EPS)
         assert np.all(np.abs(pp - want) <= 1e-6 * np.maximum(np.abs(want), 1e-3))
+
+
+# ----------------------------------------------------------- the 12-byte report
+
+def test_report_pack_layout(orc):
+    """The report read back before the update (RUDA docs "Training and saving
+    state", native PyTorch section) is fixed by the page only in size: 12 bytes.
+    This build reads it as the fp64 sum of squares followed by the u32 count of
+    non-finite gradients, little-endian, with the count saturated at 2^32 - 1
+    (any non-zero count skips the step either way).  Pinned against the byte
+    layout that struct.pack writes for "<dI" and against hand-decoded words."""
+    cases = [(1.25, 0.0, 3), (math.pi, 0.0, 0), (1.0, 0.5, 7), (5e-324, 0.0, 1),
+             (float("inf"), 0.0, 2 ** 32 - 1), (12345.678, -0.078, 65536)]
+    for total, comp, nonfinite in cases:
+        st = orc.Stats(total, comp, nonfinite, 0)
+        want = list(struct.unpack("<3I", struct.pack("<dI", total + comp, nonfinite)))
+        assert orc.report_pack(st) == want, (total, comp, nonfinite)
+    # hand-decoded: 1.25 = 0x3FF4000000000000; pi = 0x400921FB54442D18
+    assert orc.report_pack(orc.Stats(1.25, 0.0, 3, 0)) == [0x00000000, 0x3FF40000, 3]
+    assert orc.report_pack(orc.Stats(math.pi, 0.0, 9, 0)) == [0x54442D18, 0x400921FB, 9]
+    # the value packed is the compensated sum (sum + compensation)
+    assert orc.report_pack(orc.Stats(1.0, 0.5, 0, 0))[:2] == [0x00000000, 0x3FF80000]
+    # counts beyond 32 bits saturate instead of wrapping to a small (or zero) count
+    assert orc.report_pack(orc.Stats(1.0, 0.0, 2 ** 33, 0))[2] == 0xFFFFFFFF
+    assert orc.report_pack(orc.Stats(1.0, 0.0, 2 ** 32 + 5, 0))[2] == 0xFFFFFFFF
