@@ -409,3 +409,21 @@ def test_all_gather_list_errors(L, comm):
     bad = list(recv)
     bad[7] = None
     assert agl(bad) == L.ERR_MISSING_REGISTRATION
+
+
+def test_noalloc_wrapper_rejects_what_the_abi_cannot_see(L):
+    """rcc_grad_stats_noalloc takes bare pointers and one element count, so the
+    binding checks what the C call cannot: dtype, contiguity, equal sizes and
+    the report's size (all rejected before any call into the library)."""
+    import torch
+    a = torch.zeros(8)
+    rep = torch.zeros(3, dtype=torch.int32)
+    bad = [([a, torch.zeros(7)], rep, None),                       # sizes differ
+           ([a, torch.zeros(8, dtype=torch.bfloat16)], rep, None),  # not float32
+           ([a, torch.zeros(16)[::2]], rep, None),                  # not contiguous
+           ([a, a], torch.zeros(2, dtype=torch.int32), None),       # report < 12 bytes
+           ([a, a], rep, torch.zeros(9)),                           # mean of another size
+           ([], rep, None)]
+    for grads, report, mean in bad:
+        with pytest.raises(ValueError):
+            L.grad_stats_noalloc(grads, 1.0, report, mean_grad=mean)

@@ -3,13 +3,15 @@ example]: two ranks on the same device; `run` saves each rank's model and
 optimizer after the first update and performs the second; `resume` restores
 that state and performs the second update).  The resumed second update must
 reproduce the uninterrupted one exactly: parameters, moments, step count and
-GradScaler state."""
+GradScaler state.  Both are also checked against the CPU oracle run over the
+same two updates (parameters and moments within 1e-6 relative, step count and
+scaler exact), so a fault common to both runs cannot pass."""
 import numpy as np
 import pytest
 import torch
 
 from gradient_sync_rcc_gb300 import checkpoint, rcc, synth
-from gpu_util import DEV, session
+from gpu_util import DEV, session, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -41,8 +43,33 @@ def _grads(tensors, update, scale):
                                                (61, i, update, r), DEV) * scale)
 
 
+def _oracle_two_updates(orc, cfg, scale0):
+    """The oracle's state after updates 1 and 2 from the same initial
+    parameters and gradients (drawn on the device exactly as the runs draw
+    them, then copied to the host)."""
+    hp = [to_host(synth.gpu_draw("normal:0.02", n, torch.float32, (60, i), DEV))
+          for i, n in enumerate(SIZES)]
+    hm = [np.zeros(n, np.float32) for n in SIZES]
+    hv = [np.zeros(n, np.float32) for n in SIZES]
+    sc = orc.scaler_new(scale0)
+    step = 0
+    for update in (1, 2):
+        grads = [[to_host(synth.gpu_draw("normal:1e-3", n, torch.float32, (61, i, update, r), DEV)
+                          * sc.scale) for r in range(R)] for i, n in enumerate(SIZES)]
+        step, _, d = orc.grad_sync_adamw_step(
+            grads, hp, hm, hv, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps,
+            weight_decay=cfg.weight_decay, max_grad_norm=cfg.max_grad_norm, step=step,
+            scaler=sc)
+        assert d.skip == 0
+    return hp, hm, hv, step, sc
+
+
+def _close(gpu, ref):
+    return bool(np.all(np.abs(gpu.astype(np.float64) - ref) <= 1e-6 * np.maximum(np.abs(ref), 1e-3)))
+
+
 @pytest.mark.parametrize("flags", [0, rcc.ADAMW_GRAPH])
-def test_resume_reproduces_second_update(tmp_path, flags):
+def test_resume_reproduces_second_update(orc, tmp_path, flags):
     path = str(tmp_path / "collective-training-state.npz")
     # run: update 1, save, update 2
     run = _model()
@@ -77,3 +104,11 @@ def test_resume_reproduces_second_update(tmp_path, flags):
         for k in ("params", "exp_avg", "exp_avg_sq"):
             for x, y in zip(a[k], b[k]):
                 assert torch.equal(x.view(torch.int32), y.view(torch.int32)), k
+    # both against the oracle over the same two updates
+    hp, hm, hv, ostep, sc = _oracle_two_updates(orc, cfg, 65536.0)
+    assert (state2.step, state2.scale, state2.growth_tracker) == \
+        (ostep, sc.scale, sc.growth_tracker)
+    for i, t in enumerate(res):
+        for k, ref in (("params", hp), ("exp_avg", hm), ("exp_avg_sq", hv)):
+            for x in t[k]:
+                assert _close(to_host(x), ref[i]), (i, k)

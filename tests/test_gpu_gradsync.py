@@ -13,6 +13,7 @@ run with one NaN injected at step 7 (that step skipped, the scale halved);
 the sum of squares within 1e-12 relative; decisions and counters exact.
 """
 import math
+import struct
 
 import numpy as np
 import pytest
@@ -36,6 +37,21 @@ def _built():
 
 def close(gpu, ref):
     return bool(np.all(np.abs(gpu.astype(np.float64) - ref) <= REL * np.maximum(np.abs(ref), 1e-3)))
+
+
+def check_report_words(orc, rep, st):
+    """The 12 bytes the call read back, word by word against the oracle's
+    packing of its own statistics (RUDA docs, native PyTorch section: a 12-byte
+    report read back before the update): the count word exactly, the two words
+    of the fp64 sum of squares decoded within 1e-12 relative (the GPU sums in a
+    different order)."""
+    want = orc.report_pack(st)
+    got = list(rep.report_words)
+    assert got[2] == want[2], (got, want)
+    s_gpu = struct.unpack("<d", struct.pack("<2I", got[0], got[1]))[0]
+    s_orc = struct.unpack("<d", struct.pack("<2I", want[0], want[1]))[0]
+    assert abs(s_gpu - s_orc) <= 1e-12 * s_orc, (s_gpu, s_orc)
+    assert s_gpu == rep.sum_sq
 
 
 class Problem:
@@ -94,6 +110,7 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
             reports.append(rep)
             assert rep.skipped == d.skip
             assert rep.nonfinite == st.nonfinite
+            check_report_words(orc, rep, st)
             assert state.step == ostep and state.scale == sc.scale
             if not d.skip:
                 want = orc.stats_value(st)
@@ -113,8 +130,9 @@ def run_steps(orc, prob, steps, nan_at, cfg_kw, check_each=True, scale=65536.0, 
                     assert close(to_host(t["exp_avg"][0]), prob.hm[i]), (k, i)
                     assert close(to_host(t["exp_avg_sq"][0]), prob.hv[i]), (k, i)
                     for j in range(1, prob.rep):
-                        assert torch.equal(t["params"][j], t["params"][0])
-                        assert torch.equal(t["exp_avg_sq"][j], t["exp_avg_sq"][0])
+                        for key in ("params", "exp_avg", "exp_avg_sq"):
+                            assert torch.equal(t[key][j].view(torch.int32),
+                                               t[key][0].view(torch.int32)), (k, i, j, key)
     return reports, state
 
 
@@ -307,6 +325,7 @@ def test_full_1024_tensors_ten_steps(orc):
                 means.append(mean)
             d = orc.decide(st, MAXN)
             assert rep.skipped == d.skip and rep.nonfinite == st.nonfinite
+            check_report_words(orc, rep, st)
             if d.skip:
                 orc.scaler_update(sc, True)
             else:
@@ -320,13 +339,15 @@ def test_full_1024_tensors_ten_steps(orc):
             assert state.step == t and state.scale == sc.scale
             assert rep.combine_launches == _levels(rep.stats_rows)
     assert t == 9 and state.scale == 32768.0
-    bad = 0
+    bad = []
     for i in range(P):
-        if not close(to_host(p_dev[i][0]), hp[i]):
-            bad += 1
-        for j in range(1, rep_count):
-            assert torch.equal(p_dev[i][j], p_dev[i][0])
-    assert bad == 0
+        for name, dev_list, ref in (("p", p_dev, hp), ("m", m_dev, hm), ("v", v_dev, hv)):
+            if not close(to_host(dev_list[i][0]), ref[i]):
+                bad.append((name, i))
+            for j in range(1, rep_count):
+                assert torch.equal(dev_list[i][j].view(torch.int32),
+                                   dev_list[i][0].view(torch.int32)), (name, i, j)
+    assert not bad, bad[:10]
     assert math.isfinite(rep.grad_norm)
 
 

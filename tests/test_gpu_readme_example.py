@@ -1,4 +1,5 @@
-"""The Python example in README.md runs as written."""
+"""The Python usage example in the repository's front-page documentation runs
+as written: one gradient-sync step applied, not skipped."""
 import os
 import re
 
@@ -16,7 +17,7 @@ def test_readme_python_example_runs(capsys):
     assert torch.cuda.is_available()
     text = open(os.path.join(ROOT, "README.md")).read()
     blocks = re.findall(r"```python\n(.*?)```", text, re.S)
-    assert blocks, "README has no python example"
+    assert blocks, "no python example found"
     scope = {}
     exec(compile(blocks[0], "README.md", "exec"), scope)
     torch.cuda.synchronize()
