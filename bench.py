@@ -11,8 +11,17 @@ that batch:
   grad_sync_adamw: the 8 rank buffers as the gradients of one 2^24-element
     parameter tensor -> mean, unscale, fan-in-1024 statistics, 12-byte report,
     clip, AdamW update (one fp32 state copy)
-Metric: algorithm GB/s = sum over the step's rows of R*N*bytes / step time.
+Metric (value): all_reduce algorithm GB/s = 3 * R*N*bytes / (time of the
+step's three all_reduce rows).  The whole step's algorithm bandwidth over all
+eight rows is reported beside it (step_algbw_gbs).
 Every input (512 MiB per row) exceeds the 129 MB L2, so no flush is needed.
+
+After the timed step the same line carries, each timed on its own:
+  bf16_rs_ag_8x2p26  reduce_scatter then all_gather, 8 ranks x 2^26 bf16 per
+                     rank (shard 2^23), fp32 accumulation
+  grad_sync_1024     gradient sync + AdamW over 4 ranks and 1024 fp32 tensors
+                     (sizes log-uniform in [1024, 4194304]), default flow, with
+                     4 state copies (one per rank) and with 1
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 For N > 1 launch under torchrun: each rank runs the same workload on its own
@@ -22,6 +31,7 @@ barriers and the max over ranks is reported.
 import argparse
 import hashlib
 import json
+import math
 import os
 import platform
 import re
@@ -65,6 +75,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave out the bf16 RS/AG and 1024-tensor grad-sync legs of the line")
     ap.add_argument("--case", default="step",
                     choices=["step", "all_reduce", "reduce", "broadcast", "reduce_scatter",
                              "all_gather", "all_to_all", "grad_sync", "grad_sync_1024"],
@@ -281,12 +293,14 @@ class Workload:
         return rep
 
 
-def e2e_leg(torch, rcc, wl, h, K):
+def e2e_leg(torch, rcc, wl, h, K, ar_only=False):
     """End to end through the public API with host buffers: every step copies
     its R input buffers from pinned host memory and reads a result back
-    (rank 0's all_reduce output and, inside the call, the 12-byte report).
-    Inputs are double-buffered: step k+1's copies run on four copy streams
-    while step k computes.  Returns ms per step."""
+    (rank 0's all_reduce output and, in the whole step, inside the grad-sync
+    call, the 12-byte report).  ar_only: the step is the three all_reduce rows
+    (the metric's rows); otherwise all eight rows.  Inputs are double-buffered:
+    step k+1's copies run on four copy streams while step k computes.  Returns
+    ms per step."""
     sets_in = [wl.ins, [torch.empty_like(x) for x in wl.ins]]
     gs_sets = [wl.sets, rcc.ParamSets([dict(wl.gs_tensors[0], grads=sets_in[1])])]
     host_in = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(R)]
@@ -319,7 +333,11 @@ def e2e_leg(torch, rcc, wl, h, K):
             issue_copy(k + 1)
         for ev in copied[b]:
             main.wait_event(ev)
-        wl.step(h, ins=sets_in[b], sets=gs_sets[b])
+        if ar_only:
+            for op in ("sum", "mean", "max"):
+                rcc.all_reduce(h, sets_in[b], wl.ar, op)
+        else:
+            wl.step(h, ins=sets_in[b], sets=gs_sets[b])
         consumed[b].record(main)
         used[b] = True
         host_out.copy_(wl.ar[0], non_blocking=True)
@@ -343,6 +361,92 @@ def copy_bandwidth(torch, device):
     ms = s.elapsed_time(e) / 10
     del a, b
     return 2 * (1 << 31) / (ms * 1e-3) / 1e9
+
+
+def timed_median(torch, fn, K, warm=3):
+    """Median of K CUDA-event-timed calls of fn on the current stream."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev[0].record()
+    for k in range(K):
+        fn()
+        ev[k + 1].record()
+    torch.cuda.synchronize()
+    return statistics.median(ev[k].elapsed_time(ev[k + 1]) for k in range(K))
+
+
+def _row(ms, alg_bytes, traffic, peak, src):
+    gbs = traffic / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "algbw_gbs": round(alg_bytes / (ms * 1e-3) / 1e9, 1),
+            "min_traffic_bytes": traffic, "traffic_gbs": round(gbs, 1),
+            "frac_of_" + src: round(gbs / peak, 4)}
+
+
+def bf16_rs_ag_leg(torch, rcc, dev_index, device, peak, src, K=10):
+    """reduce_scatter then all_gather, 8 ranks x 2^26 bf16 per rank, N(0, 1)
+    inputs, fp32 accumulation, rank-order sums; each collective timed alone
+    (median of K).  Minimum traffic (R + 1) * N * 2 bytes for both."""
+    from gradient_sync_rcc_gb300 import synth
+    R3, N3 = 8, 1 << 26
+    n3 = N3 // R3
+    ins = synth.gpu_rank_buffers("normal1", R3, N3, torch.bfloat16, (300,), device)
+    rs = [torch.empty(n3, dtype=torch.bfloat16, device=device) for _ in range(R3)]
+    ag = [torch.empty(N3, dtype=torch.bfloat16, device=device) for _ in range(R3)]
+    h = rcc.register(dev_index, R3, rcc.BF16, True)
+    try:
+        rs_ms = timed_median(torch, lambda: rcc.reduce_scatter(h, ins, rs, "sum"), K)
+        ag_ms = timed_median(torch, lambda: rcc.all_gather(h, rs, ag), K)
+    finally:
+        rcc.finish(h)
+    traffic = (R3 + 1) * N3 * 2
+    return {"workload": "8 ranks x 2^26 bf16 per rank (shard 2^23), N(0,1), fp32 accumulation, "
+                        "rank order; median of %d launches each" % K,
+            "reduce_scatter": _row(rs_ms, R3 * N3 * 2, traffic, peak, src),
+            "all_gather": _row(ag_ms, R3 * N3 * 2, traffic, peak, src)}
+
+
+def grad_sync_1024_leg(torch, rcc, dev_index, device, peak, src, K=5, replicas=(4, 1)):
+    """Gradient sync + AdamW: 4 ranks, 1024 fp32 tensors with sizes
+    log-uniform in [1024, 4194304] (429,088,269 elements), grads
+    N(0, 1e-3) x 65536, lr 1e-3, betas (0.9, 0.999), eps 1e-8, wd 0.01,
+    max_grad_norm 1.0, the mean gradient stored; default flow (report read
+    back, decision on the host, one update launch per tensor).  Per state-copy
+    count: 3 untimed steps, then the median of K CUDA-event-timed steps.
+    Minimum traffic per element (4R + 4) + (4 + 24 * replicas) bytes."""
+    from gradient_sync_rcc_gb300 import synth
+    Rk, P = 4, 1024
+    sizes = synth.param_sizes(P, 1024, 4194304, 20)
+    E = sum(sizes)
+    grads = [[synth.gpu_draw("normal:1e-3", n, torch.float32, (22, i, 1, r), device) * 65536.0
+              for r in range(Rk)] for i, n in enumerate(sizes)]
+    means = [torch.empty(n, device=device) for n in sizes]
+    out = {"workload": "4 ranks, 1024 fp32 tensors log-uniform in [1024, 4194304], %d elements, "
+                       "default flow, median of %d steps after 3" % (E, K)}
+    for rep in replicas:
+        tensors = []
+        for i, n in enumerate(sizes):
+            p0 = synth.gpu_draw("normal:0.02", n, torch.float32, (21, i), device)
+            tensors.append(dict(grads=grads[i], params=[p0] + [p0.clone() for _ in range(rep - 1)],
+                                exp_avg=[torch.zeros(n, device=device) for _ in range(rep)],
+                                exp_avg_sq=[torch.zeros(n, device=device) for _ in range(rep)],
+                                mean_grad=means[i]))
+        sets = rcc.ParamSets(tensors)
+        cfg = rcc.adamw_cfg(replicas=rep)
+        state = rcc.optim_state(scale=65536.0)
+        h = rcc.register(dev_index, Rk, rcc.F32, True)
+        try:
+            ms = timed_median(torch, lambda: rcc.grad_sync_adamw(h, sets, cfg, state), K)
+        finally:
+            rcc.finish(h)
+        traffic = (Rk * 4 + 4) * E + (4 + 24 * rep) * E
+        row = _row(ms, Rk * E * 4, traffic, peak, src)
+        row.pop("algbw_gbs")
+        out["replicas_%d" % rep] = row
+        del tensors, sets
+        torch.cuda.empty_cache()
+    return out
 
 
 def bench_ours(args):
@@ -392,23 +496,38 @@ def bench_ours(args):
         # end to end: inputs from pinned host memory, result read back, every step
         Ke = max(3, min(K, 50))
         barrier(world)
+        e2e_ar_ms = e2e_leg(torch, rcc, wl, h, Ke, ar_only=True)
+        barrier(world)
         e2e_ms = e2e_leg(torch, rcc, wl, h, Ke)
         barrier(world)
-        copy_gbs = copy_bandwidth(torch, device)
     finally:
         rcc.finish(h)
+    peak0, src0 = peak_hbm()
+    del wl
+    torch.cuda.empty_cache()
+    extra = {}
+    if not args.no_extra:
+        extra["bf16_rs_ag_8x2p26"] = bf16_rs_ag_leg(torch, rcc, local, device, peak0, src0)
+        torch.cuda.empty_cache()
+        extra["grad_sync_1024"] = grad_sync_1024_leg(torch, rcc, local, device, peak0, src0)
+        torch.cuda.empty_cache()
+    copy_gbs = copy_bandwidth(torch, device)
 
     ms_step = ms_total / K
     alg_step = ALG_BYTES_ROW * len(ROWS)
-    max_ms, total_units = combine_ranks(ms_step, alg_step, world, device)
-    max_e2e, total_e2e = combine_ranks(e2e_ms, alg_step, world, device)
+    ar_rows = ["all_reduce_sum", "all_reduce_mean", "all_reduce_max"]
+    ar_ms_sum = sum(row_ms[r] for r in ar_rows)          # the three rows, per step
+    max_ar, total_ar = combine_ranks(ar_ms_sum, ALG_BYTES_ROW * len(ar_rows), world, device)
+    max_step, total_step = combine_ranks(ms_step, alg_step, world, device)
+    max_e2e, total_e2e = combine_ranks(e2e_ar_ms, ALG_BYTES_ROW * len(ar_rows), world, device)
+    max_e2e_step, total_e2e_step = combine_ranks(e2e_ms, alg_step, world, device)
     if rank != 0:
         return
     peak, peak_src = peak_hbm()
-    ar_ms = statistics.mean([row_ms["all_reduce_sum"], row_ms["all_reduce_mean"],
-                             row_ms["all_reduce_max"]])
+    ar_ms = ar_ms_sum / len(ar_rows)
     ar_traffic = MIN_TRAFFIC["all_reduce_sum"]
     achieved = ar_traffic / (ar_ms * 1e-3) / 1e9
+    traffic = ncu_traffic()
     rows = {}
     for name in ROWS:
         t = row_ms[name]
@@ -417,48 +536,68 @@ def bench_ours(args):
                       "traffic_gbs": round(gbs, 1), "frac_of_" + peak_src: round(gbs / peak, 4)}
     out = {
         "metric": METRIC,
-        "value": round(total_units / (max_ms * 1e-3) / 1e9, 2),
+        "value": round(total_ar / (max_ar * 1e-3) / 1e9, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
         "warmup": max(args.warmup, 3),
-        "ms_per_step": round(max_ms, 4),
+        "ms_per_step": round(max_step, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded device draws)",
         "config": {"workload": WORKLOAD, "ranks": R, "elements_per_rank": N,
-                   "rows_per_step": ROWS, "mode": "deterministic rank order",
+                   "rows_per_step": ROWS, "value_rows": ar_rows,
+                   "mode": "deterministic rank order",
                    "adamw_replicas": 1, "l2": "inputs 512 MiB per row > 129 MB L2, no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "step_algbw_gbs": round(total_step / (max_step * 1e-3) / 1e9, 2),
         "roofline": {"kernel": "all_reduce (multi-pointer pass, fp32, R=8, N=2^24)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "nominal_peak": NOMINAL_HBM_GBS, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_source": ("copied from the committed ncu summary "
+                                        "profiles/all_reduce_f32_8x2p24_ncu.md, taken on the "
+                                        "same kernel source" if traffic is not None else
+                                        "null: no ncu summary taken on this kernel source"),
                      "algorithmic_bytes_per_launch": ar_traffic,
                      "avg_launch_ms": round(ar_ms, 4)},
         "rows": rows,
         "e2e": {"value": round(total_e2e / (max_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(max_e2e, 3),
+                "what": "per step: the 8 rank inputs copied from pinned host memory, the "
+                        "step's three all_reduce rows through the C ABI, one output read back",
                 "pipeline": "inputs double-buffered; step k+1's H2D copies on 4 streams overlap step k",
-                "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES + 12},
+                "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES},
+        "e2e_step": {"value": round(total_e2e_step / (max_e2e_step * 1e-3) / 1e9, 2),
+                     "unit": "GB/s (algorithm bytes of all eight rows)",
+                     "ms_per_step": round(max_e2e_step, 3),
+                     "what": "the whole step (all eight rows) with host inputs, as e2e",
+                     "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES + 12},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "d2d_copy_gbs_measured_here": round(copy_gbs, 1),
     }
+    out.update(extra)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(target_s=10.0)
+        omp = cpu_baseline_omp(target_s=5.0)
+        if omp is not None:
+            out["cpu_baseline_omp"] = omp
     print(json.dumps(out), flush=True)
 
 
 # ------------------------------------------------------------------ the oracle on host cores
 
 def oracle_step(orc, xs, state):
-    """One pass of the step's rows over host arrays, in the oracle."""
+    """One pass of the step's rows over host arrays, in the oracle.  Returns
+    the seconds spent in the three all_reduce rows (the metric's rows)."""
     n = xs[0].size
+    t0 = time.perf_counter()
     for op in ("sum", "mean", "max"):
         orc.all_reduce(xs, op)
+    t_ar = time.perf_counter() - t0
     out = np.empty(n, np.float32)
     orc.reduce(xs, "sum", out)
     orc.broadcast(xs[0], [np.empty(n, np.float32) for _ in range(len(xs))])
@@ -469,6 +608,7 @@ def oracle_step(orc, xs, state):
                                        eps=1e-8, weight_decay=0.01, max_grad_norm=1.0, step=t,
                                        scaler=sc)
     state[4] = t
+    return t_ar
 
 
 def host_info():
@@ -505,20 +645,53 @@ def _oracle_setup(n):
 
 
 def cpu_baseline(target_s=10.0, n=1 << 22):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    workload: the step's eight rows over 8 ranks x n fp32; value in the
+    metric's terms (the three all_reduce rows), the whole step beside it."""
     orc, xs, state = _oracle_setup(n)
-    reps = 0
+    reps, t_ar = 0, 0.0
     t0 = time.perf_counter()
     while True:
-        oracle_step(orc, xs, state)
+        t_ar += oracle_step(orc, xs, state)
         reps += 1
         el = time.perf_counter() - t0
         if el >= target_s:
             break
-    alg = R * n * ES * len(ROWS) * reps
-    return {"value": round(alg / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(3 * R * n * ES * reps / t_ar / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "host": host_info(),
+            "step_algbw_gbs": round(R * n * ES * len(ROWS) * reps / el / 1e9, 4),
+            "sample": "the step's 8 rows over 8 ranks x 2^%d fp32 (1/%d of the workload), "
+                      "%d passes, %.1f s single-threaded; value over the three all_reduce rows"
+                      % (int(math.log2(n)), N // n, reps, el)}
+
+
+def cpu_baseline_omp(target_s=5.0, n=1 << 22):
+    """A second CPU baseline: the oracle's fp32 rank-order all_reduce
+    arithmetic written with an OpenMP loop over elements, on every host core
+    (oracle/rcc_oracle_omp.cpp; not part of the oracle's reference path).
+    None if it cannot be built here."""
+    try:
+        import oracle.omp as omp
+        lib = omp.lib()
+    except Exception:
+        return None
+    from gradient_sync_rcc_gb300 import synth
+    xs = synth.rank_buffers("grad", R, n, 2, 3)
+    outs = [np.empty(n, np.float32) for _ in range(R)]
+    threads = os.cpu_count() or 1
+    reps, t_ar = 0, 0.0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < target_s:
+        for op in ("sum", "mean", "max"):
+            t1 = time.perf_counter()
+            omp.all_reduce(xs, outs, op, threads)
+            t_ar += time.perf_counter() - t1
+        reps += 1
+    return {"value": round(3 * R * n * ES * reps / t_ar / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "kind": "oracle arithmetic, OpenMP over elements",
             "host": host_info(),
-            "sample": "the step's 8 rows over 8 ranks x 2^22 fp32 (1/4 of the workload), "
-                      "%d passes, %.1f s single-threaded" % (reps, el)}
+            "sample": "the three all_reduce rows over 8 ranks x 2^%d fp32, %d passes on %d "
+                      "threads" % (int(math.log2(n)), reps, threads)}
 
 
 def bench_reference(args):
@@ -536,24 +709,27 @@ def bench_reference(args):
     orc, xs, state = _oracle_setup(n)
     for _ in range(max(args.warmup, 3)):
         oracle_step(orc, xs, state)
+    t_ar = 0.0
     t0 = time.perf_counter()
     for _ in range(K):
-        oracle_step(orc, xs, state)
+        t_ar += oracle_step(orc, xs, state)
     el = time.perf_counter() - t0
     ms = el * 1e3 / K
-    value = R * n * ES * len(ROWS) / (ms * 1e-3) / 1e9
+    value = 3 * R * n * ES * K / t_ar / 1e9
+    step_value = R * n * ES * len(ROWS) / (ms * 1e-3) / 1e9
+    sample = ("each step: the 8 rows over 8 ranks x 2^%d fp32 (1/%d of the workload), "
+              "single-threaded; value over the three all_reduce rows" % (20 - shift, 16 << shift))
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
            "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded host draws)",
            "config": {"workload": WORKLOAD, "ranks": R, "elements_per_rank": N,
-                      "rows_per_step": ROWS, "mode": "deterministic rank order"},
+                      "rows_per_step": ROWS, "value_rows": ["all_reduce_sum", "all_reduce_mean",
+                                                            "all_reduce_max"],
+                      "mode": "deterministic rank order"},
+           "step_algbw_gbs": round(step_value, 4),
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                            "kind": "oracle",
-                            "host": host_info(),
-                            "sample": "each step: the 8 rows over 8 ranks x 2^%d fp32 "
-                                      "(1/%d of the workload), single-threaded"
-                                      % (20 - shift, 16 << shift)},
+                            "kind": "oracle", "host": host_info(), "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

@@ -29,6 +29,28 @@ def test_reference_arm_prints_one_complete_line():
     assert d["cpu_baseline"]["host"]["nproc"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # value is the metric's all_reduce rows; the whole step is reported beside it
+    assert d["config"]["value_rows"] == ["all_reduce_sum", "all_reduce_mean", "all_reduce_max"]
+    assert d["step_algbw_gbs"] > 0
+
+
+def test_openmp_baseline_computes_the_oracles_all_reduce():
+    """The second CPU baseline (all host cores) reduces exactly as the
+    single-threaded oracle does, so the two timings measure the same work."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import oracle
+    import oracle.omp as omp
+    from gradient_sync_rcc_gb300 import synth
+    oracle.build.build()
+    xs = synth.rank_buffers("grad", 5, 100003, 4, 4)
+    xs[2][17] = np.nan
+    outs = [np.empty(100003, np.float32) for _ in range(5)]
+    for op in ("sum", "mean", "max", "min"):
+        omp.all_reduce(xs, outs, op, 4)
+        want = oracle.reduce_f32(xs, op)
+        for o in outs:
+            assert o.tobytes() == want.tobytes(), op
 
 
 def test_clock_sampler_keeps_only_the_timed_window(tmp_path, monkeypatch):
