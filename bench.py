@@ -88,6 +88,9 @@ def parse_args():
     ap.add_argument("--op", default="sum", choices=["sum", "mean", "max", "min"])
     ap.add_argument("--fast", action="store_true", help="pairwise-tree sums instead of rank order")
     ap.add_argument("--replicas", type=int, default=1, help="optimizer-state copies (grad_sync_1024)")
+    ap.add_argument("--hier", type=int, default=None, choices=[0, 1, 2],
+                    help="grad-sync statistics levels: 1 combine kernels, 2 inside the "
+                         "statistics kernel, 0 flat (default: the binding's default)")
     ap.add_argument("--elems-per-row", type=int, default=0,
                     help="statistics row size for the grad-sync cases (0: the library default)")
     ap.add_argument("--sweep", action="store_true",
@@ -735,6 +738,10 @@ def bench_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def hier_kw(args):
+    return {} if args.hier is None else {"hierarchical_stats": args.hier}
+
+
 def gs_flags(rcc, mode):
     """`--gs-mode` -> rcc_adamw_cfg.flags."""
     return {"host": 0, "device": rcc.ADAMW_DEVICE_DECISION, "graph": rcc.ADAMW_GRAPH,
@@ -764,7 +771,7 @@ def bench_grad_sync_1024(args):
                             mean_grad=torch.empty(n, device=dev)))
     sets = rcc.ParamSets(tensors)
     cfg = rcc.adamw_cfg(replicas=rep, flags=gs_flags(rcc, args.gs_mode),
-                        elems_per_row=args.elems_per_row)
+                        elems_per_row=args.elems_per_row, **hier_kw(args))
     state = rcc.optim_state(scale=65536.0)
     h = rcc.register(0, Rk, rcc.F32, True)
     try:
@@ -866,7 +873,7 @@ def bench_case(args):
                                    exp_avg_sq=[torch.zeros_like(p0)],
                                    mean_grad=torch.empty_like(p0))])
         cfg = rcc.adamw_cfg(replicas=1, flags=gs_flags(rcc, args.gs_mode),
-                            elems_per_row=args.elems_per_row)
+                            elems_per_row=args.elems_per_row, **hier_kw(args))
         state = rcc.optim_state(scale=1.0)
         traffic = (Rk * 4 + 4) * n + 28 * n
 

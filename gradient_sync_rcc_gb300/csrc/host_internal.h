@@ -101,6 +101,35 @@ inline rcc_status wait_event(cudaEvent_t ev, const char* what) {
   }
 }
 
+// Wait (bounded, as wait_event) for the 12-byte report: the kernel that writes
+// it stores the call's sequence number to `seq_word` in the mapped host slot
+// once the report words are visible there.  `ev`, recorded after that kernel,
+// is queried between polls so that a failed kernel is reported at once; once
+// it has completed the word must hold `seq`.
+inline rcc_status wait_report_word(const uint32_t* seq_word, uint32_t seq, cudaEvent_t ev,
+                                   const char* what) {
+  const auto t0 = std::chrono::steady_clock::now();
+  const int limit = wait_limit_ms();
+  for (uint32_t polls = 0;; ++polls) {
+    if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) == seq) return RCC_OK;
+    if ((polls & 15u) == 15u) {
+      cudaError_t e = cudaEventQuery(ev);
+      if (e == cudaSuccess) {
+        if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) == seq) return RCC_OK;
+        return fail(RCC_ERR_CUDA, "%s: the report kernel completed without writing the report",
+                    what);
+      }
+      if (e != cudaErrorNotReady) return cuda_fail(e, what);
+    }
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                        std::chrono::steady_clock::now() - t0)
+                        .count();
+    if (ms > limit)
+      return fail(RCC_ERR_TIMEOUT, "%s: GPU work did not complete within %d ms", what, limit);
+    if (ms >= 20) std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
 // ---- sessions ----------------------------------------------------------------
 
 constexpr size_t kCombineRegionBytes = 49200;   // 4096 level-1 rows + 4 level-2 rows, 12 B each
@@ -113,7 +142,9 @@ struct Scratch {
   size_t rows_cap = 0;
   void* combine = nullptr;          // the reused reduction region, kCombineRegionBytes
   uint32_t* report_dev = nullptr;   // 12-byte report (16 allocated)
-  uint32_t* report_host = nullptr;  // pinned, mapped readback slot
+  uint32_t* report_host = nullptr;  // pinned, mapped readback slot: 3 report words + seq
+  uint32_t report_seq = 0;          // sequence number of the last call's report
+  uint32_t* counters = nullptr;     // in-kernel levels: kGsCounters zeroed counters
   uint32_t* report_host_dev = nullptr;  // its device alias (the report kernel writes it), or
                                         // null: then a 12-byte D2H copy fills the slot
   void* desc_dev = nullptr;         // tensor table + grad table + state table
@@ -212,6 +243,7 @@ struct ArrivalSync {
 inline void free_scratch(Scratch& s) {
   if (s.rows) cudaFree(s.rows);
   if (s.combine) cudaFree(s.combine);
+  if (s.counters) cudaFree(s.counters);
   if (s.report_dev) cudaFree(s.report_dev);
   if (s.report_host) cudaFreeHost(s.report_host);
   if (s.desc_dev) cudaFree(s.desc_dev);

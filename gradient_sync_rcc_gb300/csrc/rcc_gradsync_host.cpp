@@ -65,6 +65,8 @@ rcc_status ensure_fixed_scratch(Scratch& sc) {
   if (!sc.report_host) {
     e = cudaHostAlloc(reinterpret_cast<void**>(&sc.report_host), 16, cudaHostAllocMapped);
     if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(report)");
+    std::memset(sc.report_host, 0, 16);
+    sc.report_seq = 0;
     // the report kernel stores the 12 bytes straight into this slot, so no
     // copy is queued between the report and the host's wait
     void* alias = nullptr;
@@ -183,6 +185,9 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   if (!finite_pos(cfg->eps)) return fail(RCC_ERR_INVALID_ARGUMENT, "eps must be finite and > 0");
   if (!std::isfinite(cfg->weight_decay) || !std::isfinite(cfg->max_grad_norm))
     return fail(RCC_ERR_INVALID_ARGUMENT, "weight_decay and max_grad_norm must be finite");
+  if (cfg->hierarchical_stats < 0 || cfg->hierarchical_stats > 2)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "hierarchical_stats %d must be 0, 1 or 2",
+                cfg->hierarchical_stats);
   const uint32_t epr = cfg->elems_per_row ? cfg->elems_per_row : kDefaultElemsPerRow;
   if (epr % 4 != 0 || epr > (1u << 24))
     return fail(RCC_ERR_INVALID_ARGUMENT, "elems_per_row %u must be a multiple of 4 in [4, 2^24]",
@@ -220,6 +225,16 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     sc.stale = false;
   }
   if ((st = ensure_fixed_scratch(sc)) != RCC_OK) return st;
+  const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
+  // in-kernel levels: the last CTA of each 1024-row group combines it
+  const bool fused = cfg->hierarchical_stats == 2;
+  if (fused && !sc.counters) {
+    cudaError_t ce = cudaMalloc(reinterpret_cast<void**>(&sc.counters),
+                                rcc::kGsCounters * sizeof(uint32_t));
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaMalloc(level counters)");
+    ce = cudaMemsetAsync(sc.counters, 0, rcc::kGsCounters * sizeof(uint32_t), cs);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemsetAsync(level counters)");
+  }
   const bool timing = (s->flags.load() & RCC_STEP_TIMING) != 0;
   sc.timed = false;
   if (timing) {
@@ -336,7 +351,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   } else {
     ++sc.same_tables;
   }
-  const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
   // The default flow becomes the host-graph flow -- the same decision on the
   // host, the same kernels, the P launches replayed from a captured graph --
   // once the same tensors have come three calls in a row, for P >= 32 (below
@@ -370,6 +384,16 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   ga.elems_per_row = epr;
   ga.R = R;
   ga.inv_scale = inv_scale;
+  const uint32_t seq = ++sc.report_seq == 0 ? ++sc.report_seq : sc.report_seq;  // never 0
+  if (fused) {
+    ga.counters = sc.counters;
+    ga.region = static_cast<uint32_t*>(sc.combine);
+    ga.report = sc.report_dev;
+    ga.host_copy = sc.report_host_dev;
+    ga.seq = seq;
+    ga.decision = on_device ? sc.decision_dev : nullptr;
+    ga.max_grad_norm = cfg->max_grad_norm;
+  }
   // RCC_STEP_TIMING: an event at each phase boundary on the call's stream
   auto mark = [&](int k) -> cudaError_t {
     return timing ? cudaEventRecord(sc.time_ev[k], cs) : cudaSuccess;
@@ -382,6 +406,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   const uint32_t* src = static_cast<const uint32_t*>(sc.rows);
   uint64_t rows = total_rows;
   int levels = 0;
+  int combine_kernels = 0;
   uint64_t region_bytes = 0;
   if (cfg->hierarchical_stats) {
     uint32_t* region = static_cast<uint32_t*>(sc.combine);
@@ -389,19 +414,24 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       // level 1 writes rows [0, 4096) of the region, level 2 rows [4096, 4100)
       uint32_t* out = region + (levels == 0 ? 0 : 4096 * 3);
       const uint64_t out_rows = (rows + kFanIn - 1) / kFanIn;
-      if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
-        return cuda_fail(e, "combine kernel");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
+      if (!fused) {
+        if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
+          return cuda_fail(e, "combine kernel");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        ++combine_kernels;
+      }
       region_bytes = (levels == 0 ? 0 : 4096 * 12) + out_rows * 12;
       src = out;
       rows = out_rows;
       ++levels;
     }
   }
-  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, cs)) !=
-      cudaSuccess)
-    return cuda_fail(e, "report kernel");
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!fused) {
+    if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
+        cudaSuccess)
+      return cuda_fail(e, "report kernel");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
   if (!sc.report_host_dev &&
       (e = cudaMemcpyAsync(sc.report_host, sc.report_dev, 12, cudaMemcpyDeviceToHost, cs)) !=
           cudaSuccess)
@@ -547,11 +577,14 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
 
   uint64_t device_updates = 0;
   if (on_device) {
-    // decide on the GPU and enqueue the updates behind it, before waiting
-    if ((e = rcc::launch_gs_decide(sc.report_dev, cfg->max_grad_norm, sc.decision_dev, cs)) !=
-        cudaSuccess)
-      return cuda_fail(e, "decision kernel");
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+    // decide on the GPU (inside the statistics kernel with in-kernel levels,
+    // else one more kernel) and enqueue the updates behind it, before waiting
+    if (!fused) {
+      if ((e = rcc::launch_gs_decide(sc.report_dev, cfg->max_grad_norm, sc.decision_dev, cs)) !=
+          cudaSuccess)
+        return cuda_fail(e, "decision kernel");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
     ua.clip_coef = 1.0f;
     ua.decision = sc.decision_dev;
     ua.dev_scalars = sc.scalars_dev;
@@ -565,7 +598,10 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     device_updates = launches_per_update;
     g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
   }
-  if ((st = wait_event(sc.report_ev, "12-byte report readback")) != RCC_OK) {
+  st = sc.report_host_dev
+           ? wait_report_word(sc.report_host + 3, seq, sc.report_ev, "12-byte report readback")
+           : wait_event(sc.report_ev, "12-byte report readback");
+  if (st != RCC_OK) {
     // nothing of this step is applied by the host (default flow: no update
     // was launched); mark the queued work so that the next call waits for it
     if (cudaEventRecord(sc.done_ev, cs) == cudaSuccess) {
@@ -593,7 +629,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   rep_out.nonfinite = nonfinite;
   rep_out.skipped = skip ? 1 : 0;
   rep_out.clip_coef = skip ? 1.0f : coef;
-  rep_out.combine_launches = levels;
+  rep_out.combine_launches = combine_kernels;
+  rep_out.combine_levels = levels;
   rep_out.stats_rows = total_rows;
   rep_out.combine_region_bytes = region_bytes;
 

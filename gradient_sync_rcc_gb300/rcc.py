@@ -75,7 +75,7 @@ class StepReport(C.Structure):
                 ("nonfinite", C.c_uint32), ("skipped", C.c_int32), ("clip_coef", C.c_float),
                 ("combine_launches", C.c_int32), ("stats_rows", C.c_uint64),
                 ("combine_region_bytes", C.c_uint64), ("update_launches", C.c_uint64),
-                ("report_words", C.c_uint32 * 3)]
+                ("report_words", C.c_uint32 * 3), ("combine_levels", C.c_int32)]
 
 
 _lib = None
@@ -308,8 +308,10 @@ def all_gather_rank(comm, rank, send, recv, stream=None):
 
 def adamw_cfg(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=1.0,
               replicas=1, hierarchical_stats=True, elems_per_row=0, flags=0):
+    """hierarchical_stats: True or 1 (fan-in-1024 levels as combine kernels),
+    2 (the same levels inside the statistics kernel), False or 0 (flat)."""
     return AdamWCfg(lr, betas[0], betas[1], eps, weight_decay, max_grad_norm, replicas,
-                    1 if hierarchical_stats else 0, elems_per_row, flags)
+                    int(hierarchical_stats), elems_per_row, flags)
 
 
 def optim_state(scale=65536.0, growth_factor=2.0, backoff_factor=0.5, growth_interval=2000,

@@ -220,20 +220,54 @@ def _levels(rows):
     return 0 if rows <= 1024 else (1 if rows <= 1024 * 1024 else 2)
 
 
+@pytest.mark.parametrize("hier", [1, 2])
 @pytest.mark.parametrize("epr,sizes", [
     (8192, [5000, 70000]),                 # few rows: no combine
     (64, [300000, 123457]),                # > 1024 rows: one combine level
     (4, [3000000, 1500001]),               # > 1024^2 rows: two combine levels
 ])
-def test_hierarchy_levels_and_region_bound(orc, epr, sizes):
+def test_hierarchy_levels_and_region_bound(orc, epr, sizes, hier):
+    """hier 1: each level a combine kernel; hier 2: the same levels taken by the
+    last CTA of each 1024-row group inside the statistics kernel."""
     prob = Problem(2, sizes, 13, 1, True)
-    reports, _ = run_steps(orc, prob, 2, None, {"elems_per_row": epr}, check_each=True)
+    reports, _ = run_steps(orc, prob, 2, None, {"elems_per_row": epr, "hierarchical_stats": hier},
+                           check_each=True)
     rows = sum(-(-n // epr) for n in sizes)
     for r in reports:
         assert r.stats_rows == rows
-        assert r.combine_launches == _levels(rows)
+        assert r.combine_levels == _levels(rows)
+        assert r.combine_launches == (_levels(rows) if hier == 1 else 0)
         assert r.combine_launches <= 2
         assert r.combine_region_bytes <= 49200
+
+
+@pytest.mark.parametrize("flags", [0, rcc.ADAMW_DEVICE_DECISION, rcc.ADAMW_GRAPH])
+@pytest.mark.parametrize("epr", [8192, 64, 4])
+def test_in_kernel_levels_give_the_same_bits(epr, flags):
+    """The levels inside the statistics kernel reduce in the combine and report
+    kernels' order: the same report words, decisions and state bits, over steps
+    that include a skipped one (in the device flows the decision is taken by
+    the statistics kernel's last CTA)."""
+    sizes = [300000, 123457, 1000]
+    out = {}
+    for hier in (1, 2):
+        prob = Problem(4, sizes, 33, 2, True)
+        cfg = rcc.adamw_cfg(replicas=2, flags=flags, elems_per_row=epr, hierarchical_stats=hier)
+        state = rcc.optim_state(scale=65536.0)
+        words = []
+        with session(4) as h:
+            for k in range(1, 5):
+                prob.load_grads(prob.host_grads(k, state.scale, nan_at=3))
+                rep = rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+                words.append((list(rep.report_words), rep.skipped, rep.clip_coef))
+            torch.cuda.synchronize()
+        out[hier] = (words, [torch.cat([t["params"][1], t["exp_avg"][0], t["exp_avg_sq"][1]]).cpu()
+                             for t in prob.tensors], state.step, state.scale)
+    assert out[1][0] == out[2][0]
+    assert [w[1] for w in out[1][0]] == [0, 0, 1, 0]
+    for a, b in zip(out[1][1], out[2][1]):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert out[1][2:] == out[2][2:]
 
 
 def test_flat_and_hierarchical_agree(orc):
@@ -244,7 +278,7 @@ def test_flat_and_hierarchical_agree(orc):
         reports, _ = run_steps(orc, prob, 1, None,
                                {"elems_per_row": 16, "hierarchical_stats": hier})
         out[hier] = reports[0]
-    assert out[False].combine_launches == 0 and out[True].combine_launches == 1
+    assert out[False].combine_levels == 0 and out[True].combine_levels == 1
     a, b = out[True].sum_sq, out[False].sum_sq
     assert abs(a - b) <= 1e-13 * a
 
@@ -337,7 +371,7 @@ def test_full_1024_tensors_ten_steps(orc):
                     orc.adamw_update(means[i], d.clip_coef, s, hp[i], hm[i], hv[i])
                 orc.scaler_update(sc, False)
             assert state.step == t and state.scale == sc.scale
-            assert rep.combine_launches == _levels(rep.stats_rows)
+            assert rep.combine_levels == _levels(rep.stats_rows)
     assert t == 9 and state.scale == 32768.0
     bad = []
     for i in range(P):
