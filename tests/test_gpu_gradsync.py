@@ -251,11 +251,11 @@ def test_in_kernel_levels_give_the_same_bits(epr, flags):
     sizes = [300000, 123457, 1000]
     out = {}
     for hier in (1, 2):
-        prob = Problem(4, sizes, 33, 2, True)
+        prob = Problem(2, sizes, 33, 2, True)
         cfg = rcc.adamw_cfg(replicas=2, flags=flags, elems_per_row=epr, hierarchical_stats=hier)
         state = rcc.optim_state(scale=65536.0)
         words = []
-        with session(4) as h:
+        with session(2) as h:
             for k in range(1, 5):
                 prob.load_grads(prob.host_grads(k, state.scale, nan_at=3))
                 rep = rcc.grad_sync_adamw(h, prob.sets, cfg, state)
