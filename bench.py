@@ -88,9 +88,9 @@ def parse_args():
     ap.add_argument("--op", default="sum", choices=["sum", "mean", "max", "min"])
     ap.add_argument("--fast", action="store_true", help="pairwise-tree sums instead of rank order")
     ap.add_argument("--replicas", type=int, default=1, help="optimizer-state copies (grad_sync_1024)")
-    ap.add_argument("--hier", type=int, default=None, choices=[0, 1, 2],
-                    help="grad-sync statistics levels: 1 combine kernels, 2 inside the "
-                         "statistics kernel, 0 flat (default: the binding's default)")
+    ap.add_argument("--hier", type=int, default=None, choices=[0, 1],
+                    help="grad-sync statistics: 1 fan-in-1024 combines, 0 flat "
+                         "(default: the binding's default, 1)")
     ap.add_argument("--elems-per-row", type=int, default=0,
                     help="statistics row size for the grad-sync cases (0: the library default)")
     ap.add_argument("--sweep", action="store_true",

@@ -14,10 +14,7 @@
 // Kernels (all launched with programmatic dependent launch, launch.cuh):
 //   gs_stats_kernel   all_reduce Mean of the R scaled gradients + unscale,
 //                     optional store of the mean gradient, and one 12-byte row
-//                     {sum g^2 (fp64), non-finite count (u32)} per block; with
-//                     in-kernel levels, the last CTA to finish each group of
-//                     1024 rows combines it, and the last one overall writes
-//                     the report (and the device decision)
+//                     {sum g^2 (fp64), non-finite count (u32)} per block
 //   gs_combine_kernel one fan-in-1024 combine level: 1024 rows -> 1 row
 //   gs_report_kernel  the last <= 1024 rows (or all rows, flat) -> report,
 //                     also stored to the host's mapped readback slot
@@ -187,76 +184,6 @@ __device__ __forceinline__ void decide_from_report(const uint32_t* report, doubl
   out->coef = coef;
 }
 
-// ---- the fan-in-1024 levels inside the statistics kernel -------------------
-// Each CTA, after writing its row, counts itself into its group of 1024 rows;
-// the CTA that completes a group (the last to arrive) reduces the group's rows
-// into the next level's row and arrives at that level in turn.  No CTA waits
-// for another: a CTA that is not last simply exits.  The reduction order is
-// the combine and report kernels' (thread t sums rows t, t + 256, ... of the
-// group, then the block reduction), so both forms give the same bits.
-
-// True in every thread of the CTA that brought `counter` to `expected`.  Its
-// row (written by thread 0) is made visible device-wide before it is counted;
-// the last arrival resets the counter for the next launch.
-__device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t expected) {
-  __shared__ uint32_t s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(counter, 1u);
-    const uint32_t last = (prev + 1u == expected) ? 1u : 0u;
-    if (last) {
-      atomicExch(counter, 0u);
-      __threadfence();
-    }
-    s_last = last;
-  }
-  __syncthreads();
-  return s_last != 0u;
-}
-
-// Rows [0, n) written by other CTAs of this kernel, read through L2 (.cg),
-// reduced into one row at `out` by the whole CTA.
-__device__ __forceinline__ void reduce_rows_cg(const uint32_t* in, uint64_t n, uint32_t* out) {
-  double s = 0.0;
-  uint64_t c = 0;
-  for (uint64_t r = threadIdx.x; r < n; r += kThreads) {
-    const uint32_t lo = __ldcg(in + r * 3), hi = __ldcg(in + r * 3 + 1);
-    s += __longlong_as_double((long long)(((unsigned long long)hi << 32) | lo));
-    c += __ldcg(in + r * 3 + 2);
-  }
-  block_reduce_row(s, c, out);
-}
-
-__device__ __noinline__ void fused_levels(const GsStatsArgs& a, uint64_t row) {
-  const uint32_t* src = a.rows;
-  uint64_t n = a.total_rows;
-  uint64_t idx = row;
-  uint32_t* cnt = a.counters;
-  for (int level = 0;; ++level) {
-    const uint64_t group = idx / kFanIn;
-    const uint64_t g0 = group * kFanIn;
-    const uint64_t left = n - g0;
-    const uint32_t gsize = (uint32_t)(left < (uint64_t)kFanIn ? left : (uint64_t)kFanIn);
-    if (!last_to_arrive(cnt + group, gsize)) return;
-    if (n <= (uint64_t)kFanIn) {  // one group left: its reduction is the report
-      reduce_rows_cg(src, n, a.report);
-      if (threadIdx.x == 0) {
-        if (a.decision) decide_from_report(a.report, a.max_grad_norm, a.decision);
-        if (a.host_copy) publish_report(a.report, a.host_copy, a.seq);
-      }
-      return;
-    }
-    const uint64_t ngroups = (n + kFanIn - 1) / kFanIn;
-    uint32_t* out = a.region + (level == 0 ? 0 : 4096 * 3);
-    reduce_rows_cg(src + g0 * 3, gsize, out + group * 3);
-    src = out;
-    cnt += ngroups;
-    n = ngroups;
-    idx = group;
-  }
-}
-
 // s / R rounded once.  For R a power of two the product s * (1/R) is the
 // same correctly rounded quotient -- scaling by 2^-k rounds the same real
 // number once, subnormal results included -- at a fraction of a division's
@@ -375,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(con
     if (t.mean_grad) t.mean_grad[i] = m;
   }
   block_reduce_row(acc.value(), acc.nonfinite, a.rows + row * 3);
-  if (a.counters) fused_levels(a, row);
 }
 
 __device__ __forceinline__ double row_sum(const uint32_t* r) {
@@ -663,8 +589,7 @@ __global__ void __launch_bounds__(kThreads)
     update_one(P, rep, t.mean_grad, g, a.R, i, sv);
 }
 
-// The decision kernel of the device-decision flows when the levels run as
-// separate kernels (decide_from_report above).
+// The decision kernel of the device-decision flows (decide_from_report above).
 __global__ void gs_decide_kernel(const uint32_t* __restrict__ report, double max_norm,
                                  GsDecision* __restrict__ out) {
   pdl_wait_then_release();

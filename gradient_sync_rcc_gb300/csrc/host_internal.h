@@ -144,7 +144,6 @@ struct Scratch {
   uint32_t* report_dev = nullptr;   // 12-byte report (16 allocated)
   uint32_t* report_host = nullptr;  // pinned, mapped readback slot: 3 report words + seq
   uint32_t report_seq = 0;          // sequence number of the last call's report
-  uint32_t* counters = nullptr;     // in-kernel levels: kGsCounters zeroed counters
   uint32_t* report_host_dev = nullptr;  // its device alias (the report kernel writes it), or
                                         // null: then a 12-byte D2H copy fills the slot
   void* desc_dev = nullptr;         // tensor table + grad table + state table
@@ -243,7 +242,6 @@ struct ArrivalSync {
 inline void free_scratch(Scratch& s) {
   if (s.rows) cudaFree(s.rows);
   if (s.combine) cudaFree(s.combine);
-  if (s.counters) cudaFree(s.counters);
   if (s.report_dev) cudaFree(s.report_dev);
   if (s.report_host) cudaFreeHost(s.report_host);
   if (s.desc_dev) cudaFree(s.desc_dev);

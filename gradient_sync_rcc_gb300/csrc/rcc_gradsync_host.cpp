@@ -185,8 +185,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   if (!finite_pos(cfg->eps)) return fail(RCC_ERR_INVALID_ARGUMENT, "eps must be finite and > 0");
   if (!std::isfinite(cfg->weight_decay) || !std::isfinite(cfg->max_grad_norm))
     return fail(RCC_ERR_INVALID_ARGUMENT, "weight_decay and max_grad_norm must be finite");
-  if (cfg->hierarchical_stats < 0 || cfg->hierarchical_stats > 2)
-    return fail(RCC_ERR_INVALID_ARGUMENT, "hierarchical_stats %d must be 0, 1 or 2",
+  if (cfg->hierarchical_stats < 0 || cfg->hierarchical_stats > 1)
+    return fail(RCC_ERR_INVALID_ARGUMENT, "hierarchical_stats %d must be 0 or 1",
                 cfg->hierarchical_stats);
   const uint32_t epr = cfg->elems_per_row ? cfg->elems_per_row : kDefaultElemsPerRow;
   if (epr % 4 != 0 || epr > (1u << 24))
@@ -226,15 +226,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   }
   if ((st = ensure_fixed_scratch(sc)) != RCC_OK) return st;
   const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
-  // in-kernel levels: the last CTA of each 1024-row group combines it
-  const bool fused = cfg->hierarchical_stats == 2;
-  if (fused && !sc.counters) {
-    cudaError_t ce = cudaMalloc(reinterpret_cast<void**>(&sc.counters),
-                                rcc::kGsCounters * sizeof(uint32_t));
-    if (ce != cudaSuccess) return cuda_fail(ce, "cudaMalloc(level counters)");
-    ce = cudaMemsetAsync(sc.counters, 0, rcc::kGsCounters * sizeof(uint32_t), cs);
-    if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemsetAsync(level counters)");
-  }
   const bool timing = (s->flags.load() & RCC_STEP_TIMING) != 0;
   sc.timed = false;
   if (timing) {
@@ -385,15 +376,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   ga.R = R;
   ga.inv_scale = inv_scale;
   const uint32_t seq = ++sc.report_seq == 0 ? ++sc.report_seq : sc.report_seq;  // never 0
-  if (fused) {
-    ga.counters = sc.counters;
-    ga.region = static_cast<uint32_t*>(sc.combine);
-    ga.report = sc.report_dev;
-    ga.host_copy = sc.report_host_dev;
-    ga.seq = seq;
-    ga.decision = on_device ? sc.decision_dev : nullptr;
-    ga.max_grad_norm = cfg->max_grad_norm;
-  }
   // RCC_STEP_TIMING: an event at each phase boundary on the call's stream
   auto mark = [&](int k) -> cudaError_t {
     return timing ? cudaEventRecord(sc.time_ev[k], cs) : cudaSuccess;
@@ -414,24 +396,20 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       // level 1 writes rows [0, 4096) of the region, level 2 rows [4096, 4100)
       uint32_t* out = region + (levels == 0 ? 0 : 4096 * 3);
       const uint64_t out_rows = (rows + kFanIn - 1) / kFanIn;
-      if (!fused) {
-        if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
-          return cuda_fail(e, "combine kernel");
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        ++combine_kernels;
-      }
+      if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
+        return cuda_fail(e, "combine kernel");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      ++combine_kernels;
       region_bytes = (levels == 0 ? 0 : 4096 * 12) + out_rows * 12;
       src = out;
       rows = out_rows;
       ++levels;
     }
   }
-  if (!fused) {
-    if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
-        cudaSuccess)
-      return cuda_fail(e, "report kernel");
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-  }
+  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "report kernel");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!sc.report_host_dev &&
       (e = cudaMemcpyAsync(sc.report_host, sc.report_dev, 12, cudaMemcpyDeviceToHost, cs)) !=
           cudaSuccess)
@@ -577,14 +555,11 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
 
   uint64_t device_updates = 0;
   if (on_device) {
-    // decide on the GPU (inside the statistics kernel with in-kernel levels,
-    // else one more kernel) and enqueue the updates behind it, before waiting
-    if (!fused) {
-      if ((e = rcc::launch_gs_decide(sc.report_dev, cfg->max_grad_norm, sc.decision_dev, cs)) !=
-          cudaSuccess)
-        return cuda_fail(e, "decision kernel");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
+    // decide on the GPU and enqueue the updates behind it, before waiting
+    if ((e = rcc::launch_gs_decide(sc.report_dev, cfg->max_grad_norm, sc.decision_dev, cs)) !=
+        cudaSuccess)
+      return cuda_fail(e, "decision kernel");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     ua.clip_coef = 1.0f;
     ua.decision = sc.decision_dev;
     ua.dev_scalars = sc.scalars_dev;

@@ -78,8 +78,6 @@ struct GsTensor {
                             //        a multiple of 8 elements (32-byte statistics)
 };
 
-struct GsDecision;
-
 struct GsStatsArgs {
   const GsTensor* tensors;      // [num_tensors]
   const float* const* grads;    // [num_tensors * R] grad pointer table
@@ -89,24 +87,7 @@ struct GsStatsArgs {
   uint32_t elems_per_row;
   int R;
   float inv_scale;
-  // Levels inside the kernel (counters != NULL): the last CTA to finish each
-  // group of 1024 rows reduces the group into the next level's row (level 1 at
-  // region[0..4096), level 2 at region[4096..4100), 12 bytes each); the last
-  // CTA of a level of <= 1024 rows writes the report.  NULL: the host
-  // launches the combine and report kernels instead.
-  uint32_t* counters;           // one per group per level (<= kGsCounters), all zero
-                                // between launches (the last arrival resets each)
-  uint32_t* region;             // the reused reduction region
-  uint32_t* report;             // 12-byte report in device memory
-  uint32_t* host_copy;          // mapped host slot {report words, seq}, or NULL
-  uint32_t seq;                 // written to host_copy[3] after the report words
-  GsDecision* decision;         // device-decision flows: the decision, or NULL
-  double max_grad_norm;         // for the decision
 };
-
-// Counters of the in-kernel levels: <= 4096 level-1 groups, <= 4 level-2
-// groups, one final group.
-constexpr uint32_t kGsCounters = 4096 + 4 + 1;
 
 // Statistics pass: one 12-byte row per block.
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);

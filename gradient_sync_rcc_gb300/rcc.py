@@ -308,8 +308,6 @@ def all_gather_rank(comm, rank, send, recv, stream=None):
 
 def adamw_cfg(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=1.0,
               replicas=1, hierarchical_stats=True, elems_per_row=0, flags=0):
-    """hierarchical_stats: True or 1 (fan-in-1024 levels as combine kernels),
-    2 (the same levels inside the statistics kernel), False or 0 (flat)."""
     return AdamWCfg(lr, betas[0], betas[1], eps, weight_decay, max_grad_norm, replicas,
                     int(hierarchical_stats), elems_per_row, flags)
 

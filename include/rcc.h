@@ -250,13 +250,8 @@ typedef struct {
   double lr, beta1, beta2, eps, weight_decay;
   double max_grad_norm;        /* > 0: clip when the global L2 norm exceeds it; <= 0: off */
   int32_t replicas;            /* optimizer-state copies: 1 or R (each rank its own) */
-  int32_t hierarchical_stats;  /* fan-in-1024 statistics [RUDA-T]: 1 = each level a
-                                  combine kernel (none for <= 1024 rows, at most two),
-                                  then a report kernel; 2 = the same levels and
-                                  arithmetic (the same bits), taken by the last CTA to
-                                  finish each group of 1024 rows inside the statistics
-                                  kernel, which also writes the report (no extra
-                                  launches); 0 = one flat final reduction */
+  int32_t hierarchical_stats;  /* 1: fan-in-1024 combines [RUDA-T] (none for <= 1024
+                                  rows, at most two); 0: one flat final reduction */
   uint32_t elems_per_row;      /* elements summarised per statistics row; 0 = 8192;
                                   otherwise a multiple of 4 in [4, 2^24] */
   uint32_t flags;              /* 0 (the pages' flow) or RCC_ADAMW_* bits below */
@@ -307,15 +302,15 @@ typedef struct {
   uint32_t nonfinite;          /* non-finite unscaled mean gradient elements */
   int32_t skipped;             /* 1: whole step skipped (state untouched) */
   float clip_coef;             /* multiplier applied to g (1 when not clipped) */
-  int32_t combine_launches;    /* extra hierarchical combine kernels launched (0..2;
-                                  0 with hierarchical_stats = 2) */
+  int32_t combine_launches;    /* extra hierarchical combine kernels launched (0..2) */
   uint64_t stats_rows;         /* rows written by the statistics kernel */
   uint64_t combine_region_bytes; /* bytes of the reused reduction region touched (<= 49,200) */
   uint64_t update_launches;    /* AdamW update kernels launched (num_params or 0) */
   uint32_t report_words[3];    /* the 12-byte report as read back: low and high 32-bit
                                   words of the fp64 sum of g^2, then the u32 count of
                                   non-finite g (saturated at 2^32 - 1) */
-  int32_t combine_levels;      /* fan-in-1024 levels applied (0..2), in kernels or not */
+  int32_t combine_levels;      /* fan-in-1024 levels applied (0..2); one combine
+                                  kernel each */
 } rcc_step_report;
 
 /* [ruCCL §6 + RUDA-T].  One data-parallel optimizer step over num_params

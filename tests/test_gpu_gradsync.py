@@ -220,54 +220,21 @@ def _levels(rows):
     return 0 if rows <= 1024 else (1 if rows <= 1024 * 1024 else 2)
 
 
-@pytest.mark.parametrize("hier", [1, 2])
 @pytest.mark.parametrize("epr,sizes", [
     (8192, [5000, 70000]),                 # few rows: no combine
     (64, [300000, 123457]),                # > 1024 rows: one combine level
     (4, [3000000, 1500001]),               # > 1024^2 rows: two combine levels
 ])
-def test_hierarchy_levels_and_region_bound(orc, epr, sizes, hier):
-    """hier 1: each level a combine kernel; hier 2: the same levels taken by the
-    last CTA of each 1024-row group inside the statistics kernel."""
+def test_hierarchy_levels_and_region_bound(orc, epr, sizes):
     prob = Problem(2, sizes, 13, 1, True)
-    reports, _ = run_steps(orc, prob, 2, None, {"elems_per_row": epr, "hierarchical_stats": hier},
-                           check_each=True)
+    reports, _ = run_steps(orc, prob, 2, None, {"elems_per_row": epr}, check_each=True)
     rows = sum(-(-n // epr) for n in sizes)
     for r in reports:
         assert r.stats_rows == rows
         assert r.combine_levels == _levels(rows)
-        assert r.combine_launches == (_levels(rows) if hier == 1 else 0)
+        assert r.combine_launches == _levels(rows)
         assert r.combine_launches <= 2
         assert r.combine_region_bytes <= 49200
-
-
-@pytest.mark.parametrize("flags", [0, rcc.ADAMW_DEVICE_DECISION, rcc.ADAMW_GRAPH])
-@pytest.mark.parametrize("epr", [8192, 64, 4])
-def test_in_kernel_levels_give_the_same_bits(epr, flags):
-    """The levels inside the statistics kernel reduce in the combine and report
-    kernels' order: the same report words, decisions and state bits, over steps
-    that include a skipped one (in the device flows the decision is taken by
-    the statistics kernel's last CTA)."""
-    sizes = [300000, 123457, 1000]
-    out = {}
-    for hier in (1, 2):
-        prob = Problem(2, sizes, 33, 2, True)
-        cfg = rcc.adamw_cfg(replicas=2, flags=flags, elems_per_row=epr, hierarchical_stats=hier)
-        state = rcc.optim_state(scale=65536.0)
-        words = []
-        with session(2) as h:
-            for k in range(1, 5):
-                prob.load_grads(prob.host_grads(k, state.scale, nan_at=3))
-                rep = rcc.grad_sync_adamw(h, prob.sets, cfg, state)
-                words.append((list(rep.report_words), rep.skipped, rep.clip_coef))
-            torch.cuda.synchronize()
-        out[hier] = (words, [torch.cat([t["params"][1], t["exp_avg"][0], t["exp_avg_sq"][1]]).cpu()
-                             for t in prob.tensors], state.step, state.scale)
-    assert out[1][0] == out[2][0]
-    assert [w[1] for w in out[1][0]] == [0, 0, 1, 0]
-    for a, b in zip(out[1][1], out[2][1]):
-        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
-    assert out[1][2:] == out[2][2:]
 
 
 def test_flat_and_hierarchical_agree(orc):
