@@ -75,7 +75,8 @@ class StepReport(C.Structure):
                 ("nonfinite", C.c_uint32), ("skipped", C.c_int32), ("clip_coef", C.c_float),
                 ("combine_launches", C.c_int32), ("stats_rows", C.c_uint64),
                 ("combine_region_bytes", C.c_uint64), ("update_launches", C.c_uint64),
-                ("report_words", C.c_uint32 * 3), ("combine_levels", C.c_int32)]
+                ("report_words", C.c_uint32 * 3), ("combine_levels", C.c_int32),
+                ("updates_before_readback", C.c_int32)]
 
 
 _lib = None
