@@ -15,11 +15,9 @@
 //   gs_stats_kernel   all_reduce Mean of the R scaled gradients + unscale,
 //                     optional store of the mean gradient, and one 12-byte row
 //                     {sum g^2 (fp64), non-finite count (u32)} per block
-//   gs_combine_kernel one fan-in-1024 combine level: 1024 rows -> 1 row; at
-//                     the last level its last block to finish also writes the
-//                     report (and the host's mapped readback slot)
-//   gs_report_kernel  <= 1024 rows with no combine level (or all rows, flat)
-//                     -> report, also stored to the host's mapped slot
+//   gs_combine_kernel one fan-in-1024 combine level: 1024 rows -> 1 row
+//   gs_report_kernel  the last <= 1024 rows (or all rows, flat) -> report,
+//                     also stored to the host's mapped readback slot
 //   gs_decide_kernel  the host's skip / clip decision taken on the GPU (the
 //                     device-decision flows)
 //   gs_update_kernel  one launch per tensor: clip, decoupled decay, moments,
@@ -310,34 +308,9 @@ __device__ __forceinline__ double row_sum(const uint32_t* r) {
   return __longlong_as_double((long long)(((unsigned long long)r[1] << 32) | r[0]));
 }
 
-// True in every thread of the block that brought `counter` to `expected`.
-// Thread 0 wrote the block's row; it makes the row visible device-wide before
-// counting it, and the last arrival resets the counter for the next launch.
-// No block waits for another: a block that is not last just exits.
-__device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t expected) {
-  __shared__ uint32_t s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(counter, 1u);
-    const uint32_t last = (prev + 1u == expected) ? 1u : 0u;
-    if (last) {
-      atomicExch(counter, 0u);
-      __threadfence();
-    }
-    s_last = last;
-  }
-  __syncthreads();
-  return s_last != 0u;
-}
-
-// one combine level: block b reduces rows [b*1024, min((b+1)*1024, nrows));
-// with fin.counter, the last block to finish also reduces the level's output
-// rows (written by the other blocks, read through L2) into the report, in the
-// report kernel's order (thread t sums rows t, t + 256, ...), and publishes it
+// one combine level: block b reduces rows [b*1024, min((b+1)*1024, nrows))
 __global__ void __launch_bounds__(kThreads)
-    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* out,
-                      const GsFinal fin) {
+    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out) {
   pdl_wait_then_release();
   const uint64_t r0 = (uint64_t)blockIdx.x * kFanIn;
   double s = 0.0;
@@ -351,16 +324,6 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   block_reduce_row(s, c, out + (uint64_t)blockIdx.x * 3);
-  if (fin.counter == nullptr || !last_to_arrive(fin.counter, gridDim.x)) return;
-  s = 0.0;
-  c = 0;
-  for (uint64_t r = threadIdx.x; r < gridDim.x; r += kThreads) {
-    const uint32_t lo = __ldcg(out + r * 3), hi = __ldcg(out + r * 3 + 1);
-    s += __longlong_as_double((long long)(((unsigned long long)hi << 32) | lo));
-    c += __ldcg(out + r * 3 + 2);
-  }
-  block_reduce_row(s, c, fin.report);
-  if (fin.host_copy && threadIdx.x == 0) publish_report(fin.report, fin.host_copy, fin.seq);
 }
 
 // the final reduction into the 12-byte report (one block, any row count);
@@ -675,10 +638,10 @@ cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
-                              const GsFinal& fin, cudaStream_t stream) {
+                              cudaStream_t stream) {
   const unsigned blocks = (unsigned)((nrows + gs::kFanIn - 1) / gs::kFanIn);
   return launch_kernel(gs::gs_combine_kernel, dim3(blocks), dim3(kThreads), 0, stream, in, nrows,
-                       out, fin);
+                       out);
 }
 
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
@@ -908,7 +871,7 @@ extern "C" rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_
   uint64_t n = nrows;
   if (n > (uint64_t)gs::kFanIn) {
     uint32_t* out = rows + gs::kNoAllocMaxRows * 3;
-    if ((e = launch_gs_combine(src, n, out, GsFinal{}, cs)) != cudaSuccess)
+    if ((e = launch_gs_combine(src, n, out, cs)) != cudaSuccess)
       return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
     src = out;
     n = (n + gs::kFanIn - 1) / gs::kFanIn;

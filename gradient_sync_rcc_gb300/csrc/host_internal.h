@@ -144,8 +144,6 @@ struct Scratch {
   uint32_t* report_dev = nullptr;   // 12-byte report (16 allocated)
   uint32_t* report_host = nullptr;  // pinned, mapped readback slot: 3 report words + seq
   uint32_t report_seq = 0;          // sequence number of the last call's report
-  uint32_t* final_counter = nullptr;  // the last combine level's block count (zero between
-                                      // launches)
   uint32_t* report_host_dev = nullptr;  // its device alias (the report kernel writes it), or
                                         // null: then a 12-byte D2H copy fills the slot
   void* desc_dev = nullptr;         // tensor table + grad table + state table
@@ -169,11 +167,6 @@ struct Scratch {
   rcc::AdamWScalars* scalars_host_dev = nullptr;
   rcc::GsDecision* decision_host = nullptr;   // pinned, mapped staging of a host decision
   rcc::GsDecision* decision_host_dev = nullptr;
-  // the host-decision flows' gate: the update launches wait on the GPU (a
-  // stream memory wait) until the host stores the call's report sequence
-  // number here, after its decision
-  uint32_t* gate_host = nullptr;    // pinned, mapped, 16 bytes (word 0 is the gate)
-  uint32_t* gate_dev = nullptr;     // its device alias
   // per-tensor update launches on up to kMaxBranches parallel fork/join
   // chains (chain_count() of them), also the shape of the captured graph
   static constexpr int kMaxBranches = 32;
@@ -249,7 +242,6 @@ struct ArrivalSync {
 inline void free_scratch(Scratch& s) {
   if (s.rows) cudaFree(s.rows);
   if (s.combine) cudaFree(s.combine);
-  if (s.final_counter) cudaFree(s.final_counter);
   if (s.report_dev) cudaFree(s.report_dev);
   if (s.report_host) cudaFreeHost(s.report_host);
   if (s.desc_dev) cudaFree(s.desc_dev);
@@ -260,7 +252,6 @@ inline void free_scratch(Scratch& s) {
   if (s.scalars_dev) cudaFree(s.scalars_dev);
   if (s.scalars_host) cudaFreeHost(s.scalars_host);
   if (s.decision_host) cudaFreeHost(s.decision_host);
-  if (s.gate_host) cudaFreeHost(s.gate_host);
   if (s.graph_exec) cudaGraphExecDestroy(s.graph_exec);
   if (s.capture_stream) cudaStreamDestroy(s.capture_stream);
   for (int k = 0; k < Scratch::kMaxBranches; ++k) {

@@ -3,8 +3,6 @@
 // hierarchy, the report readback, the host or device decision, and the
 // per-tensor update launches.  [ruCCL README §6; RUDA docs "Training and
 // saving state", native PyTorch section.]
-#include <cuda.h>  // the stream memory wait's types (called through the runtime's entry point)
-
 #include "host_internal.h"
 
 using namespace rcc::host;
@@ -54,17 +52,11 @@ cudaError_t upload(void* dst, const void* host, const void* alias, size_t bytes,
   return cudaMemcpyAsync(dst, host, bytes, cudaMemcpyHostToDevice, cs);
 }
 
-rcc_status ensure_fixed_scratch(Scratch& sc, cudaStream_t cs) {
+rcc_status ensure_fixed_scratch(Scratch& sc) {
   cudaError_t e;
   if (!sc.combine) {
     e = cudaMalloc(&sc.combine, kCombineRegionBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(combine region)");
-  }
-  if (!sc.final_counter) {
-    e = cudaMalloc(reinterpret_cast<void**>(&sc.final_counter), 16);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(combine counter)");
-    e = cudaMemsetAsync(sc.final_counter, 0, 16, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(combine counter)");
   }
   if (!sc.report_dev) {
     e = cudaMalloc(reinterpret_cast<void**>(&sc.report_dev), 16);
@@ -112,55 +104,8 @@ rcc_status ensure_decision_scratch(Scratch& sc) {
     e = alloc_mapped(&sc.decision_host, &sc.decision_host_dev, sizeof(rcc::GsDecision));
     if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(decision)");
   }
-  if (!sc.gate_host) {
-    e = alloc_mapped(&sc.gate_host, &sc.gate_dev, 16);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(gate)");
-    std::memset(sc.gate_host, 0, 16);
-  }
   return RCC_OK;
 }
-
-// cuStreamWaitValue32, fetched once through the runtime's driver entry point
-// (no link against the driver library); null when unavailable or when
-// RCC_GATE=0 asks for the plain host launches.
-using StreamWaitFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
-StreamWaitFn stream_wait_fn() {
-  static const StreamWaitFn fn = []() -> StreamWaitFn {
-    const char* v = std::getenv("RCC_GATE");
-    if (v && v[0] == '0') return nullptr;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !p) {
-      (void)cudaGetLastError();
-      return nullptr;
-    }
-    return reinterpret_cast<StreamWaitFn>(p);
-  }();
-  return fn;
-}
-
-// The gate of the host-decision flows.  The update launches are enqueued
-// before the host waits for the report, behind a stream wait on the gate
-// word; the host opens the gate only after it has read the report back and
-// stored its decision, which a small kernel then copies to device memory for
-// the updates.  Every way out of the call opens the gate: with the host's
-// decision when it took one, else with a skip (the queued updates then return
-// at once), so no stream is ever left waiting.
-struct Gate {
-  Scratch* sc = nullptr;
-  uint32_t seq = 0;
-  bool armed = false;
-  void open(uint32_t skip, float coef) {
-    if (!armed) return;
-    sc->decision_host->skip = skip;
-    sc->decision_host->coef = coef;
-    __atomic_store_n(sc->gate_host, seq, __ATOMIC_RELEASE);  // after the decision
-    armed = false;
-  }
-  ~Gate() { open(1u, 1.0f); }
-};
 
 // Host copy of the device decision kernel: the same IEEE double arithmetic.
 void host_decision(double sum_sq, uint32_t nonfinite, double max_grad_norm, double* norm,
@@ -279,7 +224,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     if ((st = wait_event(sc.done_ev, "the previous call's GPU work")) != RCC_OK) return st;
     sc.stale = false;
   }
-  if ((st = ensure_fixed_scratch(sc, cs)) != RCC_OK) return st;
+  if ((st = ensure_fixed_scratch(sc)) != RCC_OK) return st;
   const bool on_device = (cfg->flags & (RCC_ADAMW_DEVICE_DECISION | RCC_ADAMW_GRAPH)) != 0;
   const bool timing = (s->flags.load() & RCC_STEP_TIMING) != 0;
   sc.timed = false;
@@ -407,9 +352,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       (cfg->flags == 0 && P >= kAutoGraphMinTensors && sc.same_tables >= 2 &&
        auto_graph_enabled());
   const int64_t t_next = state->step + 1;
-  // host-decision flows: updates enqueued behind the gate, before the wait
-  const bool want_gate = !on_device && stream_wait_fn() != nullptr && sc.report_host_dev;
-  if (on_device || host_graph || want_gate) {
+  if (on_device || host_graph) {
     // the scalars of step t+1, read by the updates from device memory; used
     // only if the step is not skipped
     if ((st = ensure_decision_scratch(sc)) != RCC_OK) return st;
@@ -419,9 +362,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
                cs);
     if (e != cudaSuccess) return cuda_fail(e, "scalar upload");
   }
-  const bool gated = want_gate && sc.gate_dev && sc.decision_host_dev;
-  Gate gate;
-  gate.sc = &sc;
   const char* dbase = static_cast<const char*>(sc.desc_dev);
   const float inv_scale = (float)(1.0 / state->scale);
 
@@ -456,11 +396,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       // level 1 writes rows [0, 4096) of the region, level 2 rows [4096, 4100)
       uint32_t* out = region + (levels == 0 ? 0 : 4096 * 3);
       const uint64_t out_rows = (rows + kFanIn - 1) / kFanIn;
-      // the last level's last block writes the report (no report kernel)
-      rcc::GsFinal fin{};
-      if (out_rows <= kFanIn) fin = rcc::GsFinal{sc.final_counter, sc.report_dev,
-                                                  sc.report_host_dev, seq};
-      if ((e = rcc::launch_gs_combine(src, rows, out, fin, cs)) != cudaSuccess)
+      if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
         return cuda_fail(e, "combine kernel");
       g_launches.fetch_add(1, std::memory_order_relaxed);
       ++combine_kernels;
@@ -470,12 +406,10 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       ++levels;
     }
   }
-  if (combine_kernels == 0) {
-    if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
-        cudaSuccess)
-      return cuda_fail(e, "report kernel");
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-  }
+  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e, "report kernel");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!sc.report_host_dev &&
       (e = cudaMemcpyAsync(sc.report_host, sc.report_dev, 12, cudaMemcpyDeviceToHost, cs)) !=
           cudaSuccess)
@@ -638,28 +572,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     }
     device_updates = launches_per_update;
     g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
-  } else if (gated) {
-    // the updates wait on the GPU for the host's decision (the gate), so
-    // their launches overlap the readback instead of following it
-    if (stream_wait_fn()(reinterpret_cast<CUstream>(cs), reinterpret_cast<CUdeviceptr>(sc.gate_dev),
-                         seq, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
-      return fail(RCC_ERR_CUDA, "stream wait on the decision gate could not be enqueued");
-    gate.seq = seq;
-    gate.armed = true;
-    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
-    if ((e = upload(sc.decision_dev, sc.decision_host, sc.decision_host_dev,
-                    sizeof(rcc::GsDecision), cs)) != cudaSuccess)
-      return cuda_fail(e, "decision upload");
-    ua.clip_coef = 1.0f;
-    ua.decision = sc.decision_dev;
-    ua.dev_scalars = sc.scalars_dev;
-    if (host_graph) {
-      if ((st = replay_graph()) != RCC_OK) return st;
-    } else if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess) {
-      return cuda_fail(e, "update kernel");
-    }
-    device_updates = launches_per_update;
-    g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
   }
   st = sc.report_host_dev
            ? wait_report_word(sc.report_host + 3, seq, sc.report_ev, "12-byte report readback")
@@ -701,14 +613,12 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   rep_out.report_words[0] = sc.report_host[0];
   rep_out.report_words[1] = sc.report_host[1];
   rep_out.report_words[2] = sc.report_host[2];
-  rep_out.updates_before_readback = (on_device || gated) ? 1 : 0;
-  if (gated) gate.open(skip ? 1u : 0u, coef);  // the queued updates run with it
-  if (!on_device && !gated && (e = mark(3)) != cudaSuccess)
-    return cuda_fail(e, "cudaEventRecord(timing)");
+  rep_out.updates_before_readback = on_device ? 1 : 0;
+  if (!on_device && (e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
   if (skip) {
     state->scale *= state->backoff_factor;
     state->growth_tracker = 0;
-  } else if (on_device || gated) {
+  } else if (on_device) {
     state->step = t_next;
     state->growth_tracker += 1;
     if (state->growth_tracker >= state->growth_interval) {

@@ -91,20 +91,9 @@ struct GsStatsArgs {
 
 // Statistics pass: one 12-byte row per block.
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);
-// The last combine level can also write the report: the block that finishes
-// last (counted on `counter`) reduces the level's output rows into it, in the
-// report kernel's order, so no report kernel is launched.
-struct GsFinal {
-  uint32_t* counter;    // zero between launches (the last block resets it); NULL: a
-                        // plain combine level
-  uint32_t* report;     // 12-byte report in device memory
-  uint32_t* host_copy;  // mapped host slot {report words, seq}, or NULL
-  uint32_t seq;
-};
-
 // One fan-in-1024 combine level: ceil(nrows / 1024) output rows.
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
-                              const GsFinal& fin, cudaStream_t stream);
+                              cudaStream_t stream);
 // Copies `bytes` (a multiple of 4) from pinned host memory, given by its
 // device alias, to device memory with a kernel (no copy engine).
 cudaError_t launch_host_upload(const void* src_mapped, void* dst, size_t bytes,

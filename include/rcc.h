@@ -47,9 +47,6 @@
  *                      (1..32, default 16).
  *   RCC_AUTO_GRAPH=0   the default grad-sync flow never switches to graph
  *                      replay.
- *   RCC_GATE=0         the host-decision grad-sync flows launch their updates
- *                      after the decision instead of enqueuing them behind a
- *                      GPU-side wait.
  */
 #ifndef RCC_H
 #define RCC_H
@@ -261,14 +258,7 @@ typedef struct {
 } rcc_adamw_cfg;
 
 /* rcc_adamw_cfg.flags.  By default the call reads the 12-byte report back,
- * decides on the host, then the updates run ([RUDA-T]).  The update launches
- * are enqueued before the readback, behind a GPU-side wait (a stream memory
- * wait on a word in pinned host memory) that the host releases only after it
- * has read the report and stored its decision; a small kernel copies the
- * decision to device memory for them.  Every return path releases the wait
- * (with a skip when the host took no decision), so no stream is left
- * blocked.  RCC_GATE=0, or a driver without stream memory waits, launches the
- * updates from the host after its decision instead.  Once the same
+ * decides on the host, then launches the updates ([RUDA-T]).  Once the same
  * tensors (32 or more) come three calls in a row, the default flow replays
  * those launches from a captured graph, as RCC_ADAMW_HOST_GRAPH does
  * (RCC_AUTO_GRAPH=0 keeps plain launches); the results are the same bits.
@@ -322,9 +312,8 @@ typedef struct {
   int32_t combine_levels;      /* fan-in-1024 levels applied (0..2); one combine
                                   kernel each */
   int32_t updates_before_readback; /* 1: the update launches were enqueued before the
-                                  readback (device decision, or the host's decision
-                                  behind a GPU-side wait); a skipped step's launches
-                                  then return at once */
+                                  readback (the device-decision flows); a skipped
+                                  step's launches then return at once */
 } rcc_step_report;
 
 /* [ruCCL §6 + RUDA-T].  One data-parallel optimizer step over num_params
