@@ -199,31 +199,6 @@ __device__ __forceinline__ float mean_unscale(const float* x, int R, float inv_s
   return __fmul_rn(div_by_ranks(s, R), inv_scale);
 }
 
-// L2 prefetch of slice k of nslices of the ranges in pf (64 KiB bulk
-// requests, chunk g of the concatenated ranges going to slice g % nslices),
-// spread over the block's threads.  Each SM's bulk-copy unit serves its own
-// requests, so the slices go to many CTAs.  Nothing waits for them: the
-// update kernels that follow find the beginning of their inputs in L2.
-__device__ __forceinline__ void prefetch_l2_slice(const GsPrefetch& pf, uint32_t k,
-                                                  uint32_t nslices) {
-  constexpr uint32_t kChunk = 1u << 16;
-  uint64_t g0 = 0;  // global index of the first chunk of range i
-  for (int i = 0; i < pf.n; ++i) {
-    const char* base = static_cast<const char*>(pf.ptr[i]);
-    const uint32_t bytes = pf.bytes[i];
-    const uint64_t nchunks = (bytes + kChunk - 1) / kChunk;
-    // chunks c of this range with (g0 + c) % nslices == k, one per thread
-    uint64_t c = (k + nslices - (uint32_t)(g0 % nslices)) % nslices;
-    for (c += (uint64_t)threadIdx.x * nslices; c < nchunks; c += (uint64_t)kThreads * nslices) {
-      const uint32_t off = (uint32_t)(c * kChunk);
-      const uint32_t size = bytes - off < kChunk ? bytes - off : kChunk;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(size)
-                   : "memory");
-    }
-    g0 += nchunks;
-  }
-}
-
 // Register budget: 3 CTAs per SM at eight ranks (8 x 32-byte vectors in
 // flight per thread), 4 below that.
 template <int RC>  // RC > 0: compile-time rank count; 0: runtime (a.R)
@@ -327,20 +302,35 @@ __global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(con
     if (t.mean_grad) t.mean_grad[i] = m;
   }
   block_reduce_row(acc.value(), acc.nonfinite, a.rows + row * 3);
-  // the last CTAs to start (the kernel's draining tail) prefetch the update
-  // inputs while HBM has bandwidth to spare
-  if (a.pf.n > 0 && row + a.pf.slices >= a.total_rows)
-    prefetch_l2_slice(a.pf, (uint32_t)(row + a.pf.slices - a.total_rows), a.pf.slices);
 }
 
 __device__ __forceinline__ double row_sum(const uint32_t* r) {
   return __longlong_as_double((long long)(((unsigned long long)r[1] << 32) | r[0]));
 }
 
+// L2 prefetch of the ranges in pf, in 64 KiB bulk requests spread over the
+// block's threads.  Nothing waits for them: they fill L2 while the report
+// makes its round trip to the host, so the update kernels that follow find
+// the beginning of their inputs there.
+__device__ __forceinline__ void prefetch_l2(const GsPrefetch& pf) {
+  constexpr uint32_t kChunk = 1u << 16;
+  for (int i = 0; i < pf.n; ++i) {
+    const char* base = static_cast<const char*>(pf.ptr[i]);
+    const uint32_t bytes = pf.bytes[i];
+    for (uint32_t off = threadIdx.x * kChunk; off < bytes; off += kThreads * kChunk) {
+      const uint32_t size = bytes - off < kChunk ? bytes - off : kChunk;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(size)
+                   : "memory");
+    }
+  }
+}
+
 // one combine level: block b reduces rows [b*1024, min((b+1)*1024, nrows))
 __global__ void __launch_bounds__(kThreads)
-    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out) {
+    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out,
+                      const __grid_constant__ GsPrefetch pf) {
   pdl_wait_then_release();
+  if (blockIdx.x == 0) prefetch_l2(pf);
   const uint64_t r0 = (uint64_t)blockIdx.x * kFanIn;
   double s = 0.0;
   uint64_t c = 0;
@@ -359,8 +349,10 @@ __global__ void __launch_bounds__(kThreads)
 // thread 0, which wrote the report, also stores it to the host's mapped slot
 __global__ void __launch_bounds__(kThreads)
     gs_report_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ report,
-                     uint32_t* __restrict__ host_copy, uint32_t seq) {
+                     uint32_t* __restrict__ host_copy, uint32_t seq,
+                     const __grid_constant__ GsPrefetch pf) {
   pdl_wait_then_release();
+  prefetch_l2(pf);
   double s = 0.0;
   uint64_t c = 0;
   for (uint64_t r = threadIdx.x; r < nrows; r += kThreads) {
@@ -654,8 +646,6 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace gs
 
-int gs_sm_count() { return gs::sm_count(); }
-
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
   if (a.total_rows == 0) return cudaSuccess;
   const dim3 grid((unsigned)a.total_rows), block(kThreads);
@@ -669,16 +659,17 @@ cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
-                              cudaStream_t stream) {
+                              const GsPrefetch& pf, cudaStream_t stream) {
   const unsigned blocks = (unsigned)((nrows + gs::kFanIn - 1) / gs::kFanIn);
   return launch_kernel(gs::gs_combine_kernel, dim3(blocks), dim3(kThreads), 0, stream, in, nrows,
-                       out);
+                       out, pf);
 }
 
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
-                             uint32_t* host_copy, uint32_t seq, cudaStream_t stream) {
+                             uint32_t* host_copy, uint32_t seq, const GsPrefetch& pf,
+                             cudaStream_t stream) {
   return launch_kernel(gs::gs_report_kernel, dim3(1), dim3(kThreads), 0, stream, in, nrows, report,
-                       host_copy, seq);
+                       host_copy, seq, pf);
 }
 
 cudaError_t launch_gs_update_multi(const GsMultiUpdateArgs& a, cudaStream_t stream) {
@@ -902,13 +893,13 @@ extern "C" rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_
   uint64_t n = nrows;
   if (n > (uint64_t)gs::kFanIn) {
     uint32_t* out = rows + gs::kNoAllocMaxRows * 3;
-    if ((e = launch_gs_combine(src, n, out, cs)) != cudaSuccess)
+    if ((e = launch_gs_combine(src, n, out, GsPrefetch{}, cs)) != cudaSuccess)
       return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
     src = out;
     n = (n + gs::kFanIn - 1) / gs::kFanIn;
     ++launched;
   }
-  if ((e = launch_gs_report(src, n, report, nullptr, 0u, cs)) != cudaSuccess)
+  if ((e = launch_gs_report(src, n, report, nullptr, 0u, GsPrefetch{}, cs)) != cudaSuccess)
     return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
   add_launches(launched + 1);
   return RCC_OK;

@@ -419,10 +419,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   ga.elems_per_row = epr;
   ga.R = R;
   ga.inv_scale = inv_scale;
-  // the statistics kernel's last CTAs prefetch the beginning of the update
-  // inputs into L2 (one slice per CTA, up to one per SM)
-  ga.pf = build_prefetch(params, P, R, rep, prefetch_budget());
-  ga.pf.slices = (uint32_t)std::min<uint64_t>(total_rows, (uint64_t)rcc::gs_sm_count());
   const uint32_t seq = ++sc.report_seq == 0 ? ++sc.report_seq : sc.report_seq;  // never 0
   // RCC_STEP_TIMING: an event at each phase boundary on the call's stream
   auto mark = [&](int k) -> cudaError_t {
@@ -433,6 +429,9 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
 
+  // the first kernel after the statistics pass prefetches the beginning of
+  // the update inputs into L2 while the report travels
+  rcc::GsPrefetch pf = build_prefetch(params, P, R, rep, prefetch_budget());
   const uint32_t* src = static_cast<const uint32_t*>(sc.rows);
   uint64_t rows = total_rows;
   int levels = 0;
@@ -444,8 +443,9 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       // level 1 writes rows [0, 4096) of the region, level 2 rows [4096, 4100)
       uint32_t* out = region + (levels == 0 ? 0 : 4096 * 3);
       const uint64_t out_rows = (rows + kFanIn - 1) / kFanIn;
-      if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
+      if ((e = rcc::launch_gs_combine(src, rows, out, pf, cs)) != cudaSuccess)
         return cuda_fail(e, "combine kernel");
+      pf.n = 0;
       g_launches.fetch_add(1, std::memory_order_relaxed);
       ++combine_kernels;
       region_bytes = (levels == 0 ? 0 : 4096 * 12) + out_rows * 12;
@@ -454,7 +454,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       ++levels;
     }
   }
-  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
+  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, pf, cs)) !=
       cudaSuccess)
     return cuda_fail(e, "report kernel");
   g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -78,17 +78,6 @@ struct GsTensor {
                             //        a multiple of 8 elements (32-byte statistics)
 };
 
-// Byte ranges to bring into L2 ahead of the update kernels: the beginning of
-// their inputs.  A hint only (nothing waits for it); each range starts
-// 16-byte aligned and is a multiple of 16 bytes.
-constexpr int kMaxPrefetch = 16;
-struct GsPrefetch {
-  const void* ptr[kMaxPrefetch];
-  uint32_t bytes[kMaxPrefetch];
-  int n;
-  uint32_t slices;  // statistics kernel: its last `slices` CTAs issue one slice each
-};
-
 struct GsStatsArgs {
   const GsTensor* tensors;      // [num_tensors]
   const float* const* grads;    // [num_tensors * R] grad pointer table
@@ -98,27 +87,35 @@ struct GsStatsArgs {
   uint32_t elems_per_row;
   int R;
   float inv_scale;
-  GsPrefetch pf;                // issued by the last pf.slices CTAs after their rows
 };
-
-// SMs of the current device.
-int gs_sm_count();
 
 // Statistics pass: one 12-byte row per block.
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);
+// Byte ranges to bring into L2 while the report travels to the host and back:
+// the beginning of the update kernels' inputs.  A hint only (nothing waits for
+// it); each range starts 16-byte aligned and is a multiple of 16 bytes.
+constexpr int kMaxPrefetch = 16;
+struct GsPrefetch {
+  const void* ptr[kMaxPrefetch];
+  uint32_t bytes[kMaxPrefetch];
+  int n;
+};
 
-// One fan-in-1024 combine level: ceil(nrows / 1024) output rows.
+// One fan-in-1024 combine level: ceil(nrows / 1024) output rows; block 0 also
+// issues the L2 prefetches in `pf` (pass n = 0 for none).
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
-                              cudaStream_t stream);
+                              const GsPrefetch& pf, cudaStream_t stream);
 // Copies `bytes` (a multiple of 4) from pinned host memory, given by its
 // device alias, to device memory with a kernel (no copy engine).
 cudaError_t launch_host_upload(const void* src_mapped, void* dst, size_t bytes,
                                cudaStream_t stream);
 // Final reduction of nrows rows into the 12-byte report (one block); the
 // same 12 bytes also go to `host_copy` (a mapped pinned slot) when non-null,
-// followed by `seq` in host_copy[3] once they are visible to the host.
+// followed by `seq` in host_copy[3] once they are visible to the host.  The
+// block first issues the L2 prefetches in `pf`.
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
-                             uint32_t* host_copy, uint32_t seq, cudaStream_t stream);
+                             uint32_t* host_copy, uint32_t seq, const GsPrefetch& pf,
+                             cudaStream_t stream);
 
 struct AdamWScalars {
   float step_size;     // lr / (1 - beta1^t)
