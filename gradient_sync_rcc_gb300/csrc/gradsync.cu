@@ -308,29 +308,10 @@ __device__ __forceinline__ double row_sum(const uint32_t* r) {
   return __longlong_as_double((long long)(((unsigned long long)r[1] << 32) | r[0]));
 }
 
-// L2 prefetch of the ranges in pf, in 64 KiB bulk requests spread over the
-// block's threads.  Nothing waits for them: they fill L2 while the report
-// makes its round trip to the host, so the update kernels that follow find
-// the beginning of their inputs there.
-__device__ __forceinline__ void prefetch_l2(const GsPrefetch& pf) {
-  constexpr uint32_t kChunk = 1u << 16;
-  for (int i = 0; i < pf.n; ++i) {
-    const char* base = static_cast<const char*>(pf.ptr[i]);
-    const uint32_t bytes = pf.bytes[i];
-    for (uint32_t off = threadIdx.x * kChunk; off < bytes; off += kThreads * kChunk) {
-      const uint32_t size = bytes - off < kChunk ? bytes - off : kChunk;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(size)
-                   : "memory");
-    }
-  }
-}
-
 // one combine level: block b reduces rows [b*1024, min((b+1)*1024, nrows))
 __global__ void __launch_bounds__(kThreads)
-    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out,
-                      const __grid_constant__ GsPrefetch pf) {
+    gs_combine_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ out) {
   pdl_wait_then_release();
-  if (blockIdx.x == 0) prefetch_l2(pf);
   const uint64_t r0 = (uint64_t)blockIdx.x * kFanIn;
   double s = 0.0;
   uint64_t c = 0;
@@ -349,10 +330,8 @@ __global__ void __launch_bounds__(kThreads)
 // thread 0, which wrote the report, also stores it to the host's mapped slot
 __global__ void __launch_bounds__(kThreads)
     gs_report_kernel(const uint32_t* __restrict__ in, uint64_t nrows, uint32_t* __restrict__ report,
-                     uint32_t* __restrict__ host_copy, uint32_t seq,
-                     const __grid_constant__ GsPrefetch pf) {
+                     uint32_t* __restrict__ host_copy, uint32_t seq) {
   pdl_wait_then_release();
-  prefetch_l2(pf);
   double s = 0.0;
   uint64_t c = 0;
   for (uint64_t r = threadIdx.x; r < nrows; r += kThreads) {
@@ -659,17 +638,16 @@ cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
-                              const GsPrefetch& pf, cudaStream_t stream) {
+                              cudaStream_t stream) {
   const unsigned blocks = (unsigned)((nrows + gs::kFanIn - 1) / gs::kFanIn);
   return launch_kernel(gs::gs_combine_kernel, dim3(blocks), dim3(kThreads), 0, stream, in, nrows,
-                       out, pf);
+                       out);
 }
 
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
-                             uint32_t* host_copy, uint32_t seq, const GsPrefetch& pf,
-                             cudaStream_t stream) {
+                             uint32_t* host_copy, uint32_t seq, cudaStream_t stream) {
   return launch_kernel(gs::gs_report_kernel, dim3(1), dim3(kThreads), 0, stream, in, nrows, report,
-                       host_copy, seq, pf);
+                       host_copy, seq);
 }
 
 cudaError_t launch_gs_update_multi(const GsMultiUpdateArgs& a, cudaStream_t stream) {
@@ -893,13 +871,13 @@ extern "C" rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_
   uint64_t n = nrows;
   if (n > (uint64_t)gs::kFanIn) {
     uint32_t* out = rows + gs::kNoAllocMaxRows * 3;
-    if ((e = launch_gs_combine(src, n, out, GsPrefetch{}, cs)) != cudaSuccess)
+    if ((e = launch_gs_combine(src, n, out, cs)) != cudaSuccess)
       return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
     src = out;
     n = (n + gs::kFanIn - 1) / gs::kFanIn;
     ++launched;
   }
-  if ((e = launch_gs_report(src, n, report, nullptr, 0u, GsPrefetch{}, cs)) != cudaSuccess)
+  if ((e = launch_gs_report(src, n, report, nullptr, 0u, cs)) != cudaSuccess)
     return set_error(RCC_ERR_CUDA, cudaGetErrorString(e));
   add_launches(launched + 1);
   return RCC_OK;

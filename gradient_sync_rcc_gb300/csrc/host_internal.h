@@ -78,18 +78,6 @@ inline int chain_count() {
   return n;
 }
 
-// Bytes of update inputs that the first kernel after the statistics pass
-// prefetches into L2 while the report makes its host round trip:
-// RCC_PREFETCH_MB (default 64; 0 turns it off).
-inline uint64_t prefetch_budget() {
-  static const uint64_t b = [] {
-    const char* v = std::getenv("RCC_PREFETCH_MB");
-    const long mb = v ? std::atol(v) : 64;
-    return (uint64_t)(mb < 0 ? 0 : (mb > 1024 ? 1024 : mb)) << 20;
-  }();
-  return b;
-}
-
 // Wait for an event with a time limit; never blocks forever.  Polls with
 // yields for the first 20 ms (a grad-sync readback waits for a statistics pass
 // of up to a few ms and sits on the step's critical path), then sleeps 50 us

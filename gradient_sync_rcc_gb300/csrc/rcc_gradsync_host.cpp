@@ -134,50 +134,6 @@ rcc::AdamWScalars step_scalars(const rcc_adamw_cfg* cfg, int64_t t) {
 
 bool finite_pos(double x) { return std::isfinite(x) && x > 0.0; }
 
-// The beginning of the update kernels' inputs, up to `budget` bytes, for the
-// L2 prefetch during the report's round trip: tensors largest first (the
-// order in which the update chains start), for each the gradient the update
-// reads (the mean gradient, else every rank's gradient) and every state
-// array, the same prefix of each; 16-byte aligned ranges in whole 16 bytes.
-rcc::GsPrefetch build_prefetch(const rcc_param_set* params, size_t P, int R, int rep,
-                               uint64_t budget) {
-  rcc::GsPrefetch pf{};
-  constexpr uint64_t kMinRange = 1u << 16;
-  if (budget < kMinRange) return pf;
-  std::vector<size_t> order(P);
-  for (size_t p = 0; p < P; ++p) order[p] = p;
-  std::stable_sort(order.begin(), order.end(),
-                   [&](size_t x, size_t y) { return params[x].numel > params[y].numel; });
-  for (size_t p : order) {
-    const rcc_param_set& ps = params[p];
-    std::vector<const void*> arrs;
-    if (ps.mean_grad) {
-      arrs.push_back(ps.mean_grad);
-    } else {
-      for (int r = 0; r < R; ++r) arrs.push_back(ps.grads[r]);
-    }
-    for (int k = 0; k < rep; ++k) {
-      arrs.push_back(ps.params[k]);
-      arrs.push_back(ps.exp_avg[k]);
-      arrs.push_back(ps.exp_avg_sq[k]);
-    }
-    if (pf.n + (int)arrs.size() > rcc::kMaxPrefetch) break;
-    const uint64_t share = budget / arrs.size();
-    const uint64_t whole = (uint64_t)ps.numel * sizeof(float);
-    const uint64_t take = std::min<uint64_t>(std::min(share, whole), 1ull << 30) & ~15ull;
-    if (take < kMinRange) break;
-    for (const void* a : arrs) {
-      if (!aligned16(a)) continue;
-      pf.ptr[pf.n] = a;
-      pf.bytes[pf.n] = (uint32_t)take;
-      ++pf.n;
-      budget -= take;
-    }
-    if (budget < kMinRange) break;
-  }
-  return pf;
-}
-
 }  // namespace
 
 extern "C" {
@@ -429,9 +385,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
 
-  // the first kernel after the statistics pass prefetches the beginning of
-  // the update inputs into L2 while the report travels
-  rcc::GsPrefetch pf = build_prefetch(params, P, R, rep, prefetch_budget());
   const uint32_t* src = static_cast<const uint32_t*>(sc.rows);
   uint64_t rows = total_rows;
   int levels = 0;
@@ -443,9 +396,8 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       // level 1 writes rows [0, 4096) of the region, level 2 rows [4096, 4100)
       uint32_t* out = region + (levels == 0 ? 0 : 4096 * 3);
       const uint64_t out_rows = (rows + kFanIn - 1) / kFanIn;
-      if ((e = rcc::launch_gs_combine(src, rows, out, pf, cs)) != cudaSuccess)
+      if ((e = rcc::launch_gs_combine(src, rows, out, cs)) != cudaSuccess)
         return cuda_fail(e, "combine kernel");
-      pf.n = 0;
       g_launches.fetch_add(1, std::memory_order_relaxed);
       ++combine_kernels;
       region_bytes = (levels == 0 ? 0 : 4096 * 12) + out_rows * 12;
@@ -454,7 +406,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       ++levels;
     }
   }
-  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, pf, cs)) !=
+  if ((e = rcc::launch_gs_report(src, rows, sc.report_dev, sc.report_host_dev, seq, cs)) !=
       cudaSuccess)
     return cuda_fail(e, "report kernel");
   g_launches.fetch_add(1, std::memory_order_relaxed);

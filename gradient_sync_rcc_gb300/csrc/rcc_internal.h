@@ -91,31 +91,18 @@ struct GsStatsArgs {
 
 // Statistics pass: one 12-byte row per block.
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);
-// Byte ranges to bring into L2 while the report travels to the host and back:
-// the beginning of the update kernels' inputs.  A hint only (nothing waits for
-// it); each range starts 16-byte aligned and is a multiple of 16 bytes.
-constexpr int kMaxPrefetch = 16;
-struct GsPrefetch {
-  const void* ptr[kMaxPrefetch];
-  uint32_t bytes[kMaxPrefetch];
-  int n;
-};
-
-// One fan-in-1024 combine level: ceil(nrows / 1024) output rows; block 0 also
-// issues the L2 prefetches in `pf` (pass n = 0 for none).
+// One fan-in-1024 combine level: ceil(nrows / 1024) output rows.
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
-                              const GsPrefetch& pf, cudaStream_t stream);
+                              cudaStream_t stream);
 // Copies `bytes` (a multiple of 4) from pinned host memory, given by its
 // device alias, to device memory with a kernel (no copy engine).
 cudaError_t launch_host_upload(const void* src_mapped, void* dst, size_t bytes,
                                cudaStream_t stream);
 // Final reduction of nrows rows into the 12-byte report (one block); the
 // same 12 bytes also go to `host_copy` (a mapped pinned slot) when non-null,
-// followed by `seq` in host_copy[3] once they are visible to the host.  The
-// block first issues the L2 prefetches in `pf`.
+// followed by `seq` in host_copy[3] once they are visible to the host.
 cudaError_t launch_gs_report(const uint32_t* in, uint64_t nrows, uint32_t* report,
-                             uint32_t* host_copy, uint32_t seq, const GsPrefetch& pf,
-                             cudaStream_t stream);
+                             uint32_t* host_copy, uint32_t seq, cudaStream_t stream);
 
 struct AdamWScalars {
   float step_size;     // lr / (1 - beta1^t)
