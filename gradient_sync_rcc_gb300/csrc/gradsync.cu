@@ -205,18 +205,32 @@ template <int RC>  // RC > 0: compile-time rank count; 0: runtime (a.R)
 __global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(const __grid_constant__ GsStatsArgs a) {
   pdl_wait_then_release();
   const uint64_t row = blockIdx.x;
-  // the tensor owning this row: last t with row_begin <= row
-  uint32_t lo = 0, hi = a.num_tensors - 1;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi + 1) >> 1;
-    if (a.tensors[mid].row_begin <= row)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const GsTensor t = a.tensors[lo];
   const int R = RC > 0 ? RC : a.R;
-  const float* const* g = a.grads + t.grad_slot;
+  // warp 0 finds the tensor owning this row (the last t with row_begin <=
+  // row) and stages it and its R gradient pointers in shared memory, so the
+  // descriptor loads happen once per CTA rather than once per warp
+  __shared__ GsTensor s_t;
+  __shared__ const float* s_g[kMaxRanks];
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) {
+      uint32_t lo = 0, hi = a.num_tensors - 1;
+      while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) >> 1;
+        if (a.tensors[mid].row_begin <= row)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      s_t = a.tensors[lo];
+    }
+    __syncwarp();
+    for (int q = threadIdx.x; q < R; q += 32) s_g[q] = a.grads[s_t.grad_slot + q];
+  }
+  __syncthreads();
+  const GsTensor t = s_t;
+  // read from shared memory at each use (volatile): held in registers the R
+  // pointers would push the eight-rank kernel past its register budget
+  const float* const volatile* g = s_g;
   const uint64_t c0 = (row - t.row_begin) * (uint64_t)a.elems_per_row;
   uint64_t c1 = c0 + a.elems_per_row;
   if (c1 > t.numel) c1 = t.numel;
@@ -543,15 +557,18 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
   pdl_wait();
   const int rep = REP > 0 ? REP : a.replicas;
   const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
+  // pointers from the launch arguments when the host could pass them by value
+  float* const* P = a.inl ? a.inl_state : a.state;
+  const float* const* G = a.inl ? a.inl_grads : a.grads;
   const uint64_t nv = a.vec_ok ? a.numel / W : 0;
   const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
   const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
   for (uint64_t v = tid; v < nv; v += nthreads)
-    if (!update_vec<REP, W>(a.state, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
+    if (!update_vec<REP, W>(P, rep, a.mean_grad, G, a.R, v, sv)) return;
   pdl_release();
   if (sv.d.skip) return;
   for (uint64_t i = nv * W + tid; i < a.numel; i += nthreads)
-    update_one(a.state, rep, a.mean_grad, a.grads, a.R, i, sv);
+    update_one(P, rep, a.mean_grad, G, a.R, i, sv);
 }
 
 // One launch for every tensor: block b updates statistics row b (a chunk of
