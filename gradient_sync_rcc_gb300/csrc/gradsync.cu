@@ -445,17 +445,18 @@ __device__ __forceinline__ FVec<W> ld_rw(const float* p) {
   return v;
 }
 
+// No "memory" clobber: the state loads and stores are all volatile asm, which
+// stays in program order, and without the clobber the compiler may keep the
+// tensor's pointers in registers instead of reloading them after every store.
 template <int W>
 __device__ __forceinline__ void st_rw(float* p, const FVec<W>& v) {
   if constexpr (W == 4) {
     asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.f[0]), "f"(v.f[1]),
-                 "f"(v.f[2]), "f"(v.f[3])
-                 : "memory");
+                 "f"(v.f[2]), "f"(v.f[3]));
   } else {
     asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v.f[0]),
                  "f"(v.f[1]), "f"(v.f[2]), "f"(v.f[3]), "f"(v.f[4]), "f"(v.f[5]), "f"(v.f[6]),
-                 "f"(v.f[7])
-                 : "memory");
+                 "f"(v.f[7]));
   }
 }
 
@@ -464,8 +465,11 @@ __device__ __forceinline__ void st_rw(float* p, const FVec<W>& v) {
 // state replicas are all loaded before any arithmetic; replicas beyond the
 // batch (RB: 4 with 16-byte vectors; 1 with 32-byte ones, which keeps the
 // kernel near 60 registers and 4 CTAs per SM) follow batch by batch.
-template <int REP, int W>
-__device__ __forceinline__ bool update_vec(float* const* P, int rep, const float* mean_grad,
+// P(j): the tensor's state pointer j (params 0..rep), exp_avg rep..2rep,
+// exp_avg_sq 2rep..3rep), from a table in device memory or from the launch
+// arguments.
+template <int REP, int W, typename StateAt>
+__device__ __forceinline__ bool update_vec(StateAt P, int rep, const float* mean_grad,
                                            const float* const* grads, int R, uint64_t v,
                                            const StepView& sv) {
   constexpr int RBMAX = W == 8 ? 1 : 4;
@@ -486,9 +490,9 @@ __device__ __forceinline__ bool update_vec(float* const* P, int rep, const float
 #pragma unroll
   for (int k = 0; k < RB; ++k) {
     if (k < rep) {
-      p[k] = ld_rw<W>(P[k] + off);
-      m[k] = ld_rw<W>(P[rep + k] + off);
-      w[k] = ld_rw<W>(P[2 * rep + k] + off);
+      p[k] = ld_rw<W>(P(k) + off);
+      m[k] = ld_rw<W>(P(rep + k) + off);
+      w[k] = ld_rw<W>(P(2 * rep + k) + off);
     }
   }
   if (sv.d.skip) return false;  // skipped step: state untouched
@@ -503,9 +507,9 @@ __device__ __forceinline__ bool update_vec(float* const* P, int rep, const float
 #pragma unroll
       for (int k = 0; k < RB; ++k) {
         if (r0 + k < rep) {
-          p[k] = ld_rw<W>(P[r0 + k] + off);
-          m[k] = ld_rw<W>(P[rep + r0 + k] + off);
-          w[k] = ld_rw<W>(P[2 * rep + r0 + k] + off);
+          p[k] = ld_rw<W>(P(r0 + k) + off);
+          m[k] = ld_rw<W>(P(rep + r0 + k) + off);
+          w[k] = ld_rw<W>(P(2 * rep + r0 + k) + off);
         }
       }
     }
@@ -514,9 +518,9 @@ __device__ __forceinline__ bool update_vec(float* const* P, int rep, const float
       if (r0 + k < rep) {
 #pragma unroll
         for (int e = 0; e < W; ++e) adamw_elem(g.f[e], sv.sc, p[k].f[e], m[k].f[e], w[k].f[e]);
-        st_rw<W>(P[r0 + k] + off, p[k]);
-        st_rw<W>(P[rep + r0 + k] + off, m[k]);
-        st_rw<W>(P[2 * rep + r0 + k] + off, w[k]);
+        st_rw<W>(P(r0 + k) + off, p[k]);
+        st_rw<W>(P(rep + r0 + k) + off, m[k]);
+        st_rw<W>(P(2 * rep + r0 + k) + off, w[k]);
       }
     }
   }
@@ -525,7 +529,8 @@ __device__ __forceinline__ bool update_vec(float* const* P, int rep, const float
 
 // One element of one tensor (ragged tails and unaligned tensors); the caller
 // has already checked the skip flag.
-__device__ __forceinline__ void update_one(float* const* P, int rep, const float* mean_grad,
+template <typename StateAt>
+__device__ __forceinline__ void update_one(StateAt P, int rep, const float* mean_grad,
                                            const float* const* grads, int R, uint64_t i,
                                            const StepView& sv) {
   float g;
@@ -538,11 +543,11 @@ __device__ __forceinline__ void update_one(float* const* P, int rep, const float
   }
   g = __fmul_rn(g, sv.d.coef);
   for (int r = 0; r < rep; ++r) {
-    float p = P[r][i], m = P[rep + r][i], w = P[2 * rep + r][i];
+    float p = P(r)[i], m = P(rep + r)[i], w = P(2 * rep + r)[i];
     adamw_elem(g, sv.sc, p, m, w);
-    P[r][i] = p;
-    P[rep + r][i] = m;
-    P[2 * rep + r][i] = w;
+    P(r)[i] = p;
+    P(rep + r)[i] = m;
+    P(2 * rep + r)[i] = w;
   }
 }
 
@@ -557,18 +562,26 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
   pdl_wait();
   const int rep = REP > 0 ? REP : a.replicas;
   const StepView sv = step_view(a.clip_coef, a.s, a.inv_scale, a.decision, a.dev_scalars);
-  // pointers from the launch arguments when the host could pass them by value
-  float* const* P = a.inl ? a.inl_state : a.state;
-  const float* const* G = a.inl ? a.inl_grads : a.grads;
   const uint64_t nv = a.vec_ok ? a.numel / W : 0;
   const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
   const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
-  for (uint64_t v = tid; v < nv; v += nthreads)
-    if (!update_vec<REP, W>(P, rep, a.mean_grad, G, a.R, v, sv)) return;
-  pdl_release();
-  if (sv.d.skip) return;
-  for (uint64_t i = nv * W + tid; i < a.numel; i += nthreads)
-    update_one(P, rep, a.mean_grad, G, a.R, i, sv);
+  auto body = [&](auto P) {
+    for (uint64_t v = tid; v < nv; v += nthreads)
+      if (!update_vec<REP, W>(P, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
+    pdl_release();
+    if (sv.d.skip) return;
+    for (uint64_t i = nv * W + tid; i < a.numel; i += nthreads)
+      update_one(P, rep, a.mean_grad, a.grads, a.R, i, sv);
+  };
+  // state pointers from the launch arguments (compile-time indices: constant
+  // loads, no memory requests) when the host passed them by value
+  if constexpr (REP > 0 && REP <= GsUpdateArgs::kInlineReplicas) {
+    if (a.inl) {
+      body([&](int j) { return a.inl_state[j]; });
+      return;
+    }
+  }
+  body([&](int j) { return a.state[j]; });
 }
 
 // One launch for every tensor: block b updates statistics row b (a chunk of
@@ -599,11 +612,12 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t v1 = c1 / 4;
     scalar_from = v1 * 4;
     for (uint64_t v = c0 / 4 + threadIdx.x; v < v1; v += kThreads)
-      if (!update_vec<REP, 4>(P, rep, t.mean_grad, g, a.R, v, sv)) return;
+      if (!update_vec<REP, 4>([&](int j) { return P[j]; }, rep, t.mean_grad, g, a.R, v, sv))
+        return;
   }
   if (sv.d.skip) return;
   for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads)
-    update_one(P, rep, t.mean_grad, g, a.R, i, sv);
+    update_one([&](int j) { return P[j]; }, rep, t.mean_grad, g, a.R, i, sv);
 }
 
 // The decision kernel of the device-decision flows (decide_from_report above).

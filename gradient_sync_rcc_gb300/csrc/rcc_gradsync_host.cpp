@@ -432,16 +432,13 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     ua.grads = reinterpret_cast<const float* const*>(dbase + off_grads) + p * R;
     ua.numel = params[p].numel;
     ua.vec_ok = upd_vec[p];
-    ua.inl = rep <= rcc::GsUpdateArgs::kInlineReplicas &&
-             (params[p].mean_grad || R <= rcc::GsUpdateArgs::kInlineRanks);
+    ua.inl = rep <= rcc::GsUpdateArgs::kInlineReplicas;
     if (ua.inl) {
       for (int k = 0; k < rep; ++k) {
         ua.inl_state[k] = params[p].params[k];
         ua.inl_state[rep + k] = params[p].exp_avg[k];
         ua.inl_state[2 * rep + k] = params[p].exp_avg_sq[k];
       }
-      if (!params[p].mean_grad)
-        for (int r = 0; r < R; ++r) ua.inl_grads[r] = params[p].grads[r];
     }
     return rcc::launch_gs_update(ua, where);
   };

@@ -134,14 +134,12 @@ struct GsUpdateArgs {
   AdamWScalars s;
   const GsDecision* decision;       // device decision (skip, coef); NULL: use clip_coef and s
   const AdamWScalars* dev_scalars;  // device copy of the step scalars, used with decision
-  // The same pointers by value when they fit (replicas <= 4, and a mean
-  // gradient or at most 8 ranks): read from the launch arguments instead of
-  // the tables in device memory.  inl_state has the table's layout.
+  // The state pointers by value when there are at most 4 copies: read from
+  // the launch arguments instead of the table in device memory.  inl_state
+  // has the table's layout.
   static constexpr int kInlineReplicas = 4;
-  static constexpr int kInlineRanks = 8;
   float* inl_state[3 * kInlineReplicas];
-  const float* inl_grads[kInlineRanks];
-  int inl;                          // 1: use inl_state / inl_grads
+  int inl;                          // 1: use inl_state
 };
 
 cudaError_t launch_gs_update(const GsUpdateArgs& a, cudaStream_t stream);
