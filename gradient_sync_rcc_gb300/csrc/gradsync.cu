@@ -842,6 +842,7 @@ extern "C" rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_
                                              size_t numel, double loss_scale,
                                              float* mean_grad, uint32_t* report,
                                              rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_grad_stats_noalloc");
   using namespace rcc;
   if (!grads || !report)
     return set_error(RCC_ERR_INVALID_ARGUMENT, "grads and report are required");

@@ -141,6 +141,7 @@ extern "C" {
 rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int num_params,
                                const rcc_adamw_cfg* cfg, rcc_optim_state* state,
                                rcc_step_report* report, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_grad_sync_adamw");
   t_err.clear();
   if (!params || !cfg || !state || num_params < 1)
     return fail(RCC_ERR_INVALID_ARGUMENT, "params, cfg, state and num_params >= 1 are required");
@@ -581,9 +582,12 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     device_updates = launches_per_update;
     g_launches.fetch_add(launches_per_update, std::memory_order_relaxed);
   }
-  st = sc.report_host_dev
-           ? wait_report_word(sc.report_host + 3, seq, sc.report_ev, "12-byte report readback")
-           : wait_event(sc.report_ev, "12-byte report readback");
+  {
+    rcc::NvtxRange wait_range("rcc_grad_sync_adamw: report readback");
+    st = sc.report_host_dev
+             ? wait_report_word(sc.report_host + 3, seq, sc.report_ev, "12-byte report readback")
+             : wait_event(sc.report_ev, "12-byte report readback");
+  }
   if (st != RCC_OK) {
     // nothing of this step is applied by the host (default flow: no update
     // was launched); mark the queued work so that the next call waits for it
@@ -667,6 +671,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
 }
 
 rcc_status rcc_last_step_times(rcc_comm comm, float out_ms[4]) {
+  rcc::NvtxRange nvtx_range("rcc_last_step_times");
   t_err.clear();
   if (!out_ms) return fail(RCC_ERR_INVALID_ARGUMENT, "out_ms is NULL");
   auto s = lookup(comm);

@@ -52,6 +52,7 @@ uint64_t rcc_kernel_launch_count(void) { return g_launches.load(std::memory_orde
 
 rcc_status rcc_register(int device, int num_ranks, rcc_dtype dtype, unsigned flags,
                         rcc_comm* out) {
+  rcc::NvtxRange nvtx_range("rcc_register");
   t_err.clear();
   if (!out) return fail(RCC_ERR_INVALID_ARGUMENT, "out is NULL");
   *out = nullptr;
@@ -84,6 +85,7 @@ rcc_status rcc_register(int device, int num_ranks, rcc_dtype dtype, unsigned fla
 }
 
 rcc_status rcc_set_flags(rcc_comm comm, unsigned flags) {
+  rcc::NvtxRange nvtx_range("rcc_set_flags");
   t_err.clear();
   auto s = lookup(comm);
   if (!s) return missing_session();
@@ -94,6 +96,7 @@ rcc_status rcc_set_flags(rcc_comm comm, unsigned flags) {
 }
 
 rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_finish");
   t_err.clear();
   auto s = lookup(comm);
   if (!s) return missing_session();
@@ -120,6 +123,7 @@ rcc_status rcc_finish(rcc_comm comm, rcc_stream_t stream) {
 }
 
 rcc_status rcc_reset(rcc_comm comm) {
+  rcc::NvtxRange nvtx_range("rcc_reset");
   t_err.clear();
   auto s = unregister(comm);
   if (!s) return missing_session();
@@ -182,6 +186,7 @@ extern "C" {
 
 rcc_status rcc_all_reduce(rcc_comm comm, const void* const* send, void* const* recv,
                           const size_t* counts, const rcc_op* ops, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_all_reduce");
   return all_reduce_impl(comm, send, recv, counts, ops, stream, nullptr);
 }
 
@@ -240,6 +245,7 @@ extern "C" {
 rcc_status rcc_reduce(rcc_comm comm, const void* const* send, void* const* recv,
                       const size_t* counts, const rcc_op* ops, const int* roots,
                       rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_reduce");
   return reduce_impl(comm, send, recv, counts, ops, roots, stream, nullptr);
 }
 
@@ -299,6 +305,7 @@ extern "C" {
 
 rcc_status rcc_broadcast(rcc_comm comm, const void* const* send, void* const* recv,
                          const size_t* counts, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_broadcast");
   return broadcast_impl(comm, send, recv, counts, stream, nullptr);
 }
 
@@ -356,6 +363,7 @@ extern "C" {
 
 rcc_status rcc_reduce_scatter(rcc_comm comm, const void* const* send, void* const* recv,
                               const size_t* in_counts, const rcc_op* ops, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_reduce_scatter");
   return reduce_scatter_impl(comm, send, recv, in_counts, ops, stream, nullptr);
 }
 
@@ -412,6 +420,7 @@ extern "C" {
 
 rcc_status rcc_all_gather(rcc_comm comm, const void* const* send, void* const* recv,
                           const size_t* in_counts, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_all_gather");
   return all_gather_impl(comm, send, recv, in_counts, stream, nullptr);
 }
 
@@ -419,6 +428,7 @@ rcc_status rcc_all_gather(rcc_comm comm, const void* const* send, void* const* r
 
 rcc_status rcc_all_to_all_single(rcc_comm comm, const void* const* send, void* const* recv,
                                  const size_t* in_counts, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_all_to_all_single");
   t_err.clear();
   if (!send || !recv || !in_counts)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and in_counts arrays are required");
@@ -465,6 +475,7 @@ rcc_status rcc_all_to_all_single(rcc_comm comm, const void* const* send, void* c
 
 rcc_status rcc_all_gather_list(rcc_comm comm, const void* const* send, void* const* recv,
                                const size_t* in_counts, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_all_gather_list");
   t_err.clear();
   if (!send || !recv || !in_counts)
     return fail(RCC_ERR_INVALID_ARGUMENT, "send, recv and in_counts arrays are required");

@@ -3,13 +3,37 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 
 #include "rcc.h"
 
 namespace rcc {
+
+// RCC_NVTX=1 (read once per process): every C ABI call opens an NVTX range
+// named after it, for a profiler's timeline.  Otherwise no NVTX call is made.
+inline bool nvtx_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("RCC_NVTX");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char* name) : on(nvtx_enabled()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kMaxRanks = 64;
 constexpr int kThreads = 256;  // every collective / grad-sync kernel block

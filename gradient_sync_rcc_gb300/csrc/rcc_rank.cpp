@@ -129,30 +129,35 @@ extern "C" {
 
 rcc_status rcc_all_reduce_rank(rcc_comm comm, int rank, const void* send, void* recv,
                                size_t count, rcc_op op, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_all_reduce_rank");
   return rank_arrive(comm, rank,
                      Arrival{0, send, recv, count, (int)op, 0, reinterpret_cast<cudaStream_t>(stream)});
 }
 
 rcc_status rcc_reduce_rank(rcc_comm comm, int rank, const void* send, void* recv, size_t count,
                            rcc_op op, int root, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_reduce_rank");
   return rank_arrive(comm, rank, Arrival{1, send, recv, count, (int)op, root,
                                          reinterpret_cast<cudaStream_t>(stream)});
 }
 
 rcc_status rcc_broadcast_rank(rcc_comm comm, int rank, const void* send, void* recv,
                               size_t count, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_broadcast_rank");
   return rank_arrive(comm, rank,
                      Arrival{2, send, recv, count, 0, 0, reinterpret_cast<cudaStream_t>(stream)});
 }
 
 rcc_status rcc_reduce_scatter_rank(rcc_comm comm, int rank, const void* send, void* recv,
                                    size_t in_count, rcc_op op, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_reduce_scatter_rank");
   return rank_arrive(comm, rank, Arrival{3, send, recv, in_count, (int)op, 0,
                                          reinterpret_cast<cudaStream_t>(stream)});
 }
 
 rcc_status rcc_all_gather_rank(rcc_comm comm, int rank, const void* send, void* recv,
                                size_t in_count, rcc_stream_t stream) {
+  rcc::NvtxRange nvtx_range("rcc_all_gather_rank");
   return rank_arrive(comm, rank,
                      Arrival{4, send, recv, in_count, 0, 0, reinterpret_cast<cudaStream_t>(stream)});
 }

@@ -47,6 +47,8 @@
  *                      (1..32, default 16).
  *   RCC_AUTO_GRAPH=0   the default grad-sync flow never switches to graph
  *                      replay.
+ *   RCC_NVTX=1         every call opens an NVTX range named after it (and the
+ *                      grad-sync readback wait one of its own), for a profiler.
  */
 #ifndef RCC_H
 #define RCC_H

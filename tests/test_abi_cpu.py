@@ -432,3 +432,25 @@ def test_noalloc_wrapper_rejects_what_the_abi_cannot_see(L):
     for grads, report, mean in bad:
         with pytest.raises(ValueError):
             L.grad_stats_noalloc(grads, 1.0, report, mean_grad=mean)
+
+
+def test_nvtx_ranges_do_not_change_behaviour():
+    """With RCC_NVTX=1 every call opens and closes an NVTX range (read once per
+    process, so in a child process); statuses and messages stay the same."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import ctypes as C\n"
+        "from gradient_sync_rcc_gb300 import rcc as L\n"
+        "h = C.c_void_p()\n"
+        "assert L.raw('rcc_register', 63, 4, 0, 1, C.byref(h)) == L.OK\n"
+        "assert L.raw('rcc_register', 63, 4, 0, 1, C.byref(C.c_void_p())) == "
+        "L.ERR_DUPLICATE_REGISTRATION\n"
+        "assert L.raw('rcc_set_flags', h, 0x4) == L.ERR_INVALID_ARGUMENT\n"
+        "assert L.raw('rcc_reset', h) == L.OK\n"
+        "print('nvtx ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                         env=dict(os.environ, RCC_NVTX="1"), timeout=120)
+    assert out.returncode == 0 and "nvtx ok" in out.stdout, out.stdout + out.stderr

@@ -484,3 +484,34 @@ def test_readback_timeout_applies_nothing_and_the_next_call_steps(orc, monkeypat
                              eps=EPS, weight_decay=WD, max_grad_norm=MAXN, step=0, scaler=sc)
     for i in range(len(sizes)):
         assert close(to_host(prob.tensors[i]["params"][0]), prob.hp[i])
+
+
+def test_step_times_split_the_call(orc):
+    """RCC_STEP_TIMING: the four phase times of a grad-sync call are positive and
+    add up to about the time between CUDA events around the call (the
+    statistics kernel the longest phase at this size)."""
+    sizes = [2_000_003]
+    prob = Problem(4, sizes, 34, 1, True)
+    prob.load_grads(prob.host_grads(1, 65536.0))
+    cfg = rcc.adamw_cfg(replicas=1)
+    state = rcc.optim_state(scale=65536.0)
+    h = rcc.register(0, 4, rcc.F32, True, step_timing=True)
+    try:
+        for _ in range(3):
+            rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+        b.record()
+        t = rcc.last_step_times(h)
+        torch.cuda.synchronize()
+        total = a.elapsed_time(b)
+        rcc.set_flags(h, True, step_timing=False)
+        rcc.grad_sync_adamw(h, prob.sets, cfg, state)
+        with pytest.raises(rcc.RccError):       # the last call was not timed
+            rcc.last_step_times(h)
+    finally:
+        rcc.finish(h)
+    assert all(x >= 0.0 for x in t) and t[0] > 0.0 and t[3] > 0.0, t
+    assert sum(t) <= total * 1.01 + 0.005, (t, total)
+    assert sum(t) >= 0.5 * total, (t, total)
