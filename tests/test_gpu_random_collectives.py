@@ -25,7 +25,7 @@ from gpu_util import (DEV, Guarded, bits_equal, session, tdtype, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-NCASES = 200
+NCASES = 600
 KINDS = ["all_reduce", "reduce", "broadcast", "reduce_scatter", "all_gather", "all_to_all"]
 RANKS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 33, 64]
 
