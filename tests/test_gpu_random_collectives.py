@@ -96,6 +96,10 @@ def _case(i):
     if kind in ("reduce_scatter", "all_to_all"):
         shard = int(g.integers(0, max(2, cap // R) + 1))
         n_in = R * shard
+    elif kind == "broadcast":
+        # the sender is the rank with a non-NULL buffer, and an empty tensor may
+        # have none, so broadcasts carry at least one element
+        n_in = int(g.integers(1, cap + 1))
     else:
         n_in = int(g.integers(0, cap + 1))
     specials = (det or op in ("max", "min")) and g.random() < 0.4
