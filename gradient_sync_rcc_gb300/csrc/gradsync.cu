@@ -831,7 +831,9 @@ __global__ void __launch_bounds__(kThreads)
 namespace {
 
 std::mutex g_noalloc_mu;
-uint32_t* g_noalloc_dev_ptr[256] = {};  // per device ordinal, set on first use
+// per device ordinal, set on first use and kept for the life of the process
+// (a device reset would invalidate it; the header says not to call after one)
+uint32_t* g_noalloc_dev_ptr[256] = {};
 
 bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

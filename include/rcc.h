@@ -392,6 +392,9 @@ rcc_status rcc_last_step_times(rcc_comm comm, float out_ms[4]);
  *     clearing between calls.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: a cudaDeviceReset on
+ *     that device invalidates it, so do not call this entry point after a
+ *     device reset in the same process.
  *   - Asynchronous on `stream`; no session is needed. */
 rcc_status rcc_grad_stats_noalloc(const float* const* grads, int num_ranks,
                                   size_t numel, double loss_scale,
