@@ -78,6 +78,18 @@ MUTANTS = [
      "(uint32_t)st->nonfinite", [pins.test_report_pack_layout]),
     ("report drops the compensation", "  double s = orc_stats_value(st);\n  uint64_t u;",
      "  double s = st->sum;\n  uint64_t u;", [pins.test_report_pack_layout]),
+    ("broadcast skips the last rank", "  for (int r = 0; r < R; ++r)\n    if (recv[r] != nullptr && recv[r] != root_send && bytes)",
+     "  for (int r = 0; r < R - 1; ++r)\n    if (recv[r] != nullptr && recv[r] != root_send && bytes)",
+     [lambda orc: pins.test_collective_identities(orc, "f32", 4)]),
+    ("sum of squares without compensation", "    if (std::fabs(st->sum) >= std::fabs(x))\n      st->comp += (st->sum - t) + x;\n    else\n      st->comp += (x - t) + st->sum;",
+     "", [pins.test_stats_vs_fsum]),
+    ("scaler grows one step late", "if (sc->growth_tracker >= sc->growth_interval)",
+     "if (sc->growth_tracker > sc->growth_interval)", [pins.test_scaler_growth_interval]),
+    ("max/min miss a NaN after rank 0", "    float x = xs[r];\n    if (std::isnan(x)) {\n      nan = true;",
+     "    float x = xs[r];\n    if (false) {\n      nan = true;", [pins.test_max_min_special_values]),
+    ("bf16 widening drops the sign", "float orc_bf16_to_f32(uint16_t b) { return bits_f32((uint32_t)b << 16); }",
+     "float orc_bf16_to_f32(uint16_t b) { return bits_f32((uint32_t)(b & 0x7FFFu) << 16); }",
+     [pins.test_bf16_reduce_vs_torch_and_f64]),
 ]
 
 
