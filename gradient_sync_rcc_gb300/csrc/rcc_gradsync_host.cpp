@@ -348,10 +348,14 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   // once the same tensors have come three calls in a row, for P >= 32 (below
   // that the host's launches keep pace with the GPU).
   constexpr size_t kAutoGraphMinTensors = 32;
+  const bool repeat_tables =
+      P >= kAutoGraphMinTensors && sc.same_tables >= 2 && auto_graph_enabled();
   const bool host_graph =
-      (cfg->flags & RCC_ADAMW_HOST_GRAPH) != 0 ||
-      (cfg->flags == 0 && P >= kAutoGraphMinTensors && sc.same_tables >= 2 &&
-       auto_graph_enabled());
+      (cfg->flags & RCC_ADAMW_HOST_GRAPH) != 0 || (cfg->flags == 0 && repeat_tables);
+  // likewise the device-decision flow replays its launches as RCC_ADAMW_GRAPH does
+  const bool device_graph =
+      (cfg->flags & RCC_ADAMW_GRAPH) != 0 ||
+      (cfg->flags == RCC_ADAMW_DEVICE_DECISION && repeat_tables);
   const int64_t t_next = state->step + 1;
   if (on_device || host_graph) {
     // the scalars of step t+1, read by the updates from device memory; used
@@ -573,7 +577,7 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     ua.decision = sc.decision_dev;
     ua.dev_scalars = sc.scalars_dev;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
-    if (cfg->flags & RCC_ADAMW_GRAPH) {
+    if (device_graph) {
       if ((st = replay_graph()) != RCC_OK) return st;
     } else {
       if ((e = multi ? enqueue_multi(cs) : enqueue_branched(cs)) != cudaSuccess)

@@ -268,7 +268,10 @@ typedef struct {
  *   GPU from the report (identical arithmetic: IEEE double sqrt and division,
  *   one rounding to fp32), so the per-tensor updates are enqueued right behind
  *   the statistics; a skipped step launches updates that return at once.  The
- *   report is still read back before the call returns.
+ *   report is still read back before the call returns.  Like the default flow,
+ *   it switches to replaying the per-tensor launches from a captured graph (as
+ *   RCC_ADAMW_GRAPH) once the same tensors (32 or more) come three calls in a
+ *   row (not with RCC_AUTO_GRAPH=0).
  * RCC_ADAMW_GRAPH: as DEVICE_DECISION, and the per-tensor update launches are
  *   captured once into a CUDA graph and replayed while the tensors' pointers
  *   and sizes stay the same (still one kernel node per parameter tensor).
