@@ -61,20 +61,13 @@ struct Words8 {
   uint32_t w[8];
 };
 
-// L2 policies.  Evict-first: data read or written once (the scaled
-// gradients, the optimizer state, the mean gradient on its second and last
-// read).  Evict-last: the mean gradient as the statistics pass writes it, so
-// that L2 still holds as much of it as it can when the update kernels read it
-// back right after (their evict-first loads demote the lines again).
+// An L2 policy that marks lines evict-first, for data read or written once:
+// the scaled gradients in the statistics pass, so that the mean gradient
+// written beside them is what L2 keeps; the optimizer state and the mean
+// gradient's second (last) read in the update pass.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
@@ -88,11 +81,12 @@ __device__ __forceinline__ Words8 ld_vec8(const void* p, uint64_t l2_policy) {
   return v;
 }
 
-// Write-back store with an L2 policy (the mean gradient: evict-last).
-__device__ __forceinline__ void st_vec8(void* p, const Words8& v, uint64_t l2_policy) {
-  asm volatile("st.global.L2::cache_hint.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
-               "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]),
-               "r"(v.w[6]), "r"(v.w[7]), "l"(l2_policy)
+// Write-back store: the mean gradient is read again by the update kernels
+// right after, so it is left to stay in L2 as long as it can.
+__device__ __forceinline__ void st_vec8(void* p, const Words8& v) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
                : "memory");
 }
 
@@ -253,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(con
       const uint64_t v0 = c0 / 8, v1 = c1 / 8;
       scalar_from = v1 * 8;
       const uint64_t pol = l2_evict_first_policy();
-      const uint64_t keep = l2_evict_last_policy();
       for (uint64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
         Words8 x[RC];
 #pragma unroll
@@ -268,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, RC >= 8 ? 3 : 4) gs_stats_kernel(con
           acc.add(me);
           m.w[e] = __float_as_uint(me);
         }
-        if (t.mean_grad) st_vec8(t.mean_grad + v * 8, m, keep);
+        if (t.mean_grad) st_vec8(t.mean_grad + v * 8, m);
       }
     }
   }
@@ -471,25 +464,6 @@ __device__ __forceinline__ void st_rw(float* p, const FVec<W>& v, uint64_t pol) 
   }
 }
 
-// A skipped step reads nothing, so the mean-gradient lines that the statistics
-// pass stored evict-last are read once here with the evict-first policy
-// instead, which leaves L2 to the caller's next kernels.  One 4-byte load per
-// 32-byte sector of [begin, end): elements begin, begin + 8, ... lie in
-// consecutive sectors, and the last element covers the final one.  Threads
-// `first` of `stride`.
-__device__ __forceinline__ void release_mean(const float* mean, uint64_t begin, uint64_t end,
-                                             uint64_t first, uint64_t stride) {
-  const uint64_t pol = l2_evict_first_policy();
-  auto touch = [&](const float* q) {
-    uint32_t w;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.b32 %0, [%1], %2;"
-                 : "=r"(w)
-                 : "l"(q), "l"(pol));
-  };
-  for (uint64_t i = begin + first * 8; i < end; i += stride * 8) touch(mean + i);
-  if (first == 0 && end > begin) touch(mean + end - 1);
-}
-
 // Elements [W*v, W*v + W) of one tensor.  Returns false (having written
 // nothing) when the step is skipped.  The gradient and the first batch of
 // state replicas are all loaded before any arithmetic; replicas beyond the
@@ -598,12 +572,9 @@ __global__ void __launch_bounds__(kThreads) gs_update_kernel(const __grid_consta
   const uint64_t nthreads = (uint64_t)gridDim.x * kThreads;
   auto body = [&](auto P) {
     for (uint64_t v = tid; v < nv; v += nthreads)
-      if (!update_vec<REP, W>(P, rep, a.mean_grad, a.grads, a.R, v, sv)) break;
+      if (!update_vec<REP, W>(P, rep, a.mean_grad, a.grads, a.R, v, sv)) return;
     pdl_release();
-    if (sv.d.skip) {
-      if (a.mean_grad) release_mean(a.mean_grad, 0, a.numel, tid, nthreads);
-      return;
-    }
+    if (sv.d.skip) return;
     for (uint64_t i = nv * W + tid; i < a.numel; i += nthreads)
       update_one(P, rep, a.mean_grad, a.grads, a.R, i, sv);
   };
@@ -647,12 +618,9 @@ __global__ void __launch_bounds__(kThreads)
     scalar_from = v1 * 4;
     for (uint64_t v = c0 / 4 + threadIdx.x; v < v1; v += kThreads)
       if (!update_vec<REP, 4>([&](int j) { return P[j]; }, rep, t.mean_grad, g, a.R, v, sv))
-        break;
+        return;
   }
-  if (sv.d.skip) {
-    if (t.mean_grad) release_mean(t.mean_grad, c0, c1, threadIdx.x, kThreads);
-    return;
-  }
+  if (sv.d.skip) return;
   for (uint64_t i = scalar_from + threadIdx.x; i < c1; i += kThreads)
     update_one([&](int j) { return P[j]; }, rep, t.mean_grad, g, a.R, i, sv);
 }
@@ -663,27 +631,6 @@ __global__ void gs_decide_kernel(const uint32_t* __restrict__ report, double max
   pdl_wait_then_release();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   decide_from_report(report, max_norm, out);
-}
-
-// The host flows' skipped step: block b releases the mean gradient of
-// statistics row b (the statistics kernel's partition).
-__global__ void __launch_bounds__(kThreads) gs_release_kernel(const __grid_constant__ GsStatsArgs a) {
-  pdl_wait_then_release();
-  const uint64_t row = blockIdx.x;
-  uint32_t lo = 0, hi = a.num_tensors - 1;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi + 1) >> 1;
-    if (a.tensors[mid].row_begin <= row)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const GsTensor t = a.tensors[lo];
-  if (!t.mean_grad) return;
-  const uint64_t c0 = (row - t.row_begin) * (uint64_t)a.elems_per_row;
-  uint64_t c1 = c0 + a.elems_per_row;
-  if (c1 > t.numel) c1 = t.numel;
-  release_mean(t.mean_grad, c0, c1, threadIdx.x, kThreads);
 }
 
 int sm_count() {
@@ -724,12 +671,6 @@ cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream) {
     case 8: return launch_kernel(gs::gs_stats_kernel<8>, grid, block, 0, stream, a);
     default: return launch_kernel(gs::gs_stats_kernel<0>, grid, block, 0, stream, a);
   }
-}
-
-cudaError_t launch_gs_release(const GsStatsArgs& a, cudaStream_t stream) {
-  if (a.total_rows == 0) return cudaSuccess;
-  return launch_kernel(gs::gs_release_kernel, dim3((unsigned)a.total_rows), dim3(kThreads), 0,
-                       stream, a);
 }
 
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,

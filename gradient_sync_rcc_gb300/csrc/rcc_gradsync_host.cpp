@@ -269,9 +269,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
     return !(v && std::atoi(v) == 16);
   }();
   const bool rows8 = wide_ok && epr % 8 == 0;
-  // some mean gradient goes through the 32-byte statistics path, which
-  // stores it evict-last in L2 for the update kernels
-  bool kept_mean = false;
   uint64_t row = 0;
   for (size_t p = 0; p < P; ++p) {
     const rcc_param_set& ps = params[p];
@@ -284,7 +281,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
       grads32 = grads32 && aligned32(ps.grads[r]);
     }
     gv32 = gv32 && grads32;
-    kept_mean = kept_mean || (ps.mean_grad != nullptr && gv32);
     bool uv = gv;
     // 32-byte update vectors: the gradient the update reads (the mean
     // gradient, else every rank's) and every state pointer 32-byte aligned
@@ -635,12 +631,6 @@ rcc_status rcc_grad_sync_adamw(rcc_comm comm, const rcc_param_set* params, int n
   rep_out.report_words[2] = sc.report_host[2];
   rep_out.updates_before_readback = on_device ? 1 : 0;
   if (!on_device && (e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing)");
-  if (skip && !on_device && kept_mean) {
-    // no update kernel reads the mean gradients back on this step
-    if ((e = rcc::launch_gs_release(ga, cs)) != cudaSuccess)
-      return cuda_fail(e, "mean-gradient release kernel");
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-  }
   if (skip) {
     state->scale *= state->backoff_factor;
     state->growth_tracker = 0;

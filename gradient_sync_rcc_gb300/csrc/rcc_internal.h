@@ -115,10 +115,6 @@ struct GsStatsArgs {
 
 // Statistics pass: one 12-byte row per block.
 cudaError_t launch_gs_stats(const GsStatsArgs& a, cudaStream_t stream);
-// A skipped step in the host flows: reads the mean gradients once with an
-// evict-first L2 policy (the statistics pass stored them evict-last for the
-// update kernels, which a skipped step does not launch).
-cudaError_t launch_gs_release(const GsStatsArgs& a, cudaStream_t stream);
 // One fan-in-1024 combine level: ceil(nrows / 1024) output rows.
 cudaError_t launch_gs_combine(const uint32_t* in, uint64_t nrows, uint32_t* out,
                               cudaStream_t stream);
