@@ -12,8 +12,10 @@ that batch:
     parameter tensor -> mean, unscale, fan-in-1024 statistics, 12-byte report,
     clip, AdamW update (one fp32 state copy)
 Metric (value): all_reduce algorithm GB/s = 3 * R*N*bytes / (time of the
-step's three all_reduce rows).  The whole step's algorithm bandwidth over all
-eight rows is reported beside it (step_algbw_gbs).
+step's three all_reduce rows), those rows launched K times back to back
+between one CUDA-event pair.  The whole step (K steps of all eight rows, also
+back to back) is reported beside it (ms_per_step, step_algbw_gbs); a separate
+pass with an event between rows gives the per-row breakdown (rows).
 Every input (512 MiB per row) exceeds the 129 MB L2, so no flush is needed.
 
 After the timed step the same line carries, each timed on its own:
@@ -179,9 +181,13 @@ def ncu_traffic():
 
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # Only the reasons bitmask is queried: the first process on a fresh box that
+    # also queried the four per-reason fields saw the GPU stall 60-140 ms about
+    # a second into a timed region with no idle gaps.  The bits are NVML's
+    # clocks-event reasons.
+    FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index):
         self.index = index
@@ -197,6 +203,15 @@ class ClockSampler:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def close(self):
+        """Ends the child if it still runs (stop() has not been reached)."""
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
 
     def lines(self):
         """Sample lines written so far (the file is shared with the child)."""
@@ -220,21 +235,21 @@ class ClockSampler:
         all_lines = self.f.read().splitlines()
         window = "timed region"
         chosen = all_lines[first_line:]
-        if not any(len(l.split(",")) >= 7 for l in chosen):
+        if not any(len(l.split(",")) >= 3 for l in chosen):
             chosen, window = all_lines, "load pre-roll and timed region"
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in chosen:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 3:
                 continue
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
+                mask = int(parts[2], 16)
             except ValueError:
                 continue
-            for name, val in zip(names, parts[3:7]):
-                if val.lower().startswith("active"):
+            for bit, name in self.REASON_BITS.items():
+                if mask & bit:
                     reasons.add(name)
         if not sm:
             return None
@@ -294,6 +309,13 @@ class Workload:
         rep = rcc.grad_sync_adamw(h, sets, self.cfg, self.state)
         mark(8)
         return rep
+
+    def ar_rows(self, h):
+        """The metric's rows alone: the step's three all_reduce rows."""
+        rcc = self.rcc
+        rcc.all_reduce(h, self.ins, self.ar, "sum")
+        rcc.all_reduce(h, self.ins, self.ar, "mean")
+        rcc.all_reduce(h, self.ins, self.ar, "max")
 
 
 def e2e_leg(torch, rcc, wl, h, K, ar_only=False):
@@ -366,6 +388,24 @@ def copy_bandwidth(torch, device):
     return 2 * (1 << 31) / (ms * 1e-3) / 1e9
 
 
+def timed_batch(torch, fn, K, warm=3):
+    """Mean ms of K back-to-back calls of fn on the current stream, between one
+    pair of CUDA events.  An event recorded between two launches costs the
+    device about 2 us and breaks programmatic dependent launch (another ~2 us
+    of launch latency no longer hidden), so the collectives are timed this way;
+    the per-call median below keeps an event between calls."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / K
+
+
 def timed_median(torch, fn, K, warm=3):
     """Median of K CUDA-event-timed calls of fn on the current stream."""
     for _ in range(warm):
@@ -399,13 +439,13 @@ def bf16_rs_ag_leg(torch, rcc, dev_index, device, peak, src, K=10):
     ag = [torch.empty(N3, dtype=torch.bfloat16, device=device) for _ in range(R3)]
     h = rcc.register(dev_index, R3, rcc.BF16, True)
     try:
-        rs_ms = timed_median(torch, lambda: rcc.reduce_scatter(h, ins, rs, "sum"), K)
-        ag_ms = timed_median(torch, lambda: rcc.all_gather(h, rs, ag), K)
+        rs_ms = timed_batch(torch, lambda: rcc.reduce_scatter(h, ins, rs, "sum"), K)
+        ag_ms = timed_batch(torch, lambda: rcc.all_gather(h, rs, ag), K)
     finally:
         rcc.finish(h)
     traffic = (R3 + 1) * N3 * 2
     return {"workload": "8 ranks x 2^26 bf16 per rank (shard 2^23), N(0,1), fp32 accumulation, "
-                        "rank order; median of %d launches each" % K,
+                        "rank order; %d back-to-back launches each between one event pair" % K,
             "reduce_scatter": _row(rs_ms, R3 * N3 * 2, traffic, peak, src),
             "all_gather": _row(ag_ms, R3 * N3 * 2, traffic, peak, src)}
 
@@ -460,40 +500,66 @@ def bench_ours(args):
     torch.cuda.set_device(local)
     dist = init_dist(world, "nccl")
     device = "cuda:%d" % local
-    wl = Workload(device)
-    h = rcc.register(local, R, rcc.F32, True)
+    # The clock sampler starts first and the load pre-roll below runs until it
+    # has been up 1.5 s: on a fresh box the first nvidia-smi instance stalled
+    # a saturated GPU for 60-140 ms about a second after it started.
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_sampler = time.perf_counter()
+    h = None
     try:
+        wl = Workload(device)
+        h = rcc.register(local, R, rcc.F32, True)
         for _ in range(max(args.warmup, 3)):
             wl.step(h)
         torch.cuda.synchronize()
         K = args.steps
+        Kr = min(K, 20)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
-              for _ in range(K)]
+              for _ in range(Kr)]
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ar_start = torch.cuda.Event(enable_timing=True)
+        ar_end = torch.cuda.Event(enable_timing=True)
         # load pre-roll: keep stepping (untimed) until the clock sampler is up
-        sampler = ClockSampler(local)
-        sampler.start()
+        # and has run 1.5 s
         t_pre = time.perf_counter()
-        while sampler.proc is not None and time.perf_counter() - t_pre < 3.0:
+        while sampler.proc is not None and time.perf_counter() - t_pre < 5.0:
             for _ in range(20):
                 wl.step(h)
             torch.cuda.synchronize()
-            if sampler.lines() >= 2:
+            if sampler.lines() >= 2 and time.perf_counter() - t_sampler >= 1.5:
                 break
         first_line = sampler.lines()
+        # timed region 1: K steps, every row launched back to back
         launches0 = rcc.launch_count()
         barrier(world)
         torch.cuda.synchronize()
         start.record()
         for k in range(K):
-            wl.step(h, ev[k])
+            wl.step(h)
         end.record()
         torch.cuda.synchronize()
         barrier(world)
-        launches = rcc.launch_count() - launches0
+        # timed region 2: the metric's three all_reduce rows, K times back to back
+        launches1 = rcc.launch_count()
+        barrier(world)
+        torch.cuda.synchronize()
+        ar_start.record()
+        for k in range(K):
+            wl.ar_rows(h)
+        ar_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        launches2 = rcc.launch_count()
         clocks = sampler.stop(first_line)
         ms_total = start.elapsed_time(end)
-        row_ms = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+        ar_ms_sum = ar_start.elapsed_time(ar_end) / K      # the three rows, per iteration
+        # per-row breakdown (not a headline figure): Kr more steps with an event
+        # between rows, which adds about 2-4 us of device time to each row
+        for k in range(Kr):
+            wl.step(h, ev[k])
+        torch.cuda.synchronize()
+        row_ms = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(Kr))
                   for i, name in enumerate(ROWS)}
 
         # end to end: inputs from pinned host memory, result read back, every step
@@ -504,7 +570,9 @@ def bench_ours(args):
         e2e_ms = e2e_leg(torch, rcc, wl, h, Ke)
         barrier(world)
     finally:
-        rcc.finish(h)
+        sampler.close()
+        if h is not None:
+            rcc.finish(h)
     peak0, src0 = peak_hbm()
     del wl
     torch.cuda.empty_cache()
@@ -519,7 +587,6 @@ def bench_ours(args):
     ms_step = ms_total / K
     alg_step = ALG_BYTES_ROW * len(ROWS)
     ar_rows = ["all_reduce_sum", "all_reduce_mean", "all_reduce_max"]
-    ar_ms_sum = sum(row_ms[r] for r in ar_rows)          # the three rows, per step
     max_ar, total_ar = combine_ranks(ar_ms_sum, ALG_BYTES_ROW * len(ar_rows), world, device)
     max_step, total_step = combine_ranks(ms_step, alg_step, world, device)
     max_e2e, total_e2e = combine_ranks(e2e_ar_ms, ALG_BYTES_ROW * len(ar_rows), world, device)
@@ -554,6 +621,10 @@ def bench_ours(args):
                    "rows_per_step": ROWS, "value_rows": ar_rows,
                    "mode": "deterministic rank order",
                    "adamw_replicas": 1, "l2": "inputs 512 MiB per row > 129 MB L2, no flush",
+                   "timing": ("value: K iterations of the three all_reduce rows launched back "
+                              "to back between one CUDA-event pair; ms_per_step: K steps of "
+                              "all eight rows likewise; rows: a separate pass of min(K, 20) "
+                              "steps with an event between rows (each row about 2-4 us more)"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_algbw_gbs": round(total_step / (max_step * 1e-3) / 1e9, 2),
         "roofline": {"kernel": "all_reduce (multi-pointer pass, fp32, R=8, N=2^24)",
@@ -578,7 +649,9 @@ def bench_ours(args):
                      "ms_per_step": round(max_e2e_step, 3),
                      "what": "the whole step (all eight rows) with host inputs, as e2e",
                      "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES + 12},
-        "gpu_launches": int(launches),
+        "gpu_launches": int(launches2 - launches0),
+        "gpu_launches_per_region": {"step": int(launches1 - launches0),
+                                    "value": int(launches2 - launches1)},
         "clocks": clocks,
         "d2d_copy_gbs_measured_here": round(copy_gbs, 1),
     }
@@ -844,7 +917,10 @@ def oracle_grad_sync_sample(tensors, sizes, Rk, rep, E):
 
 
 def bench_case(args):
-    """One collective alone, timed with CUDA events; prints one JSON line."""
+    """One collective alone, timed with CUDA events; prints one JSON line.  A
+    collective's `ms` is the mean of K launches back to back (as in a stream
+    of collectives); `median_ms` keeps an event between launches, which adds
+    about 4 us to each."""
     import torch
     from gradient_sync_rcc_gb300 import build, rcc, synth
     build.build()
@@ -905,22 +981,31 @@ def bench_case(args):
             ev[k + 1].record()
         torch.cuda.synchronize()
         ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+        # a collective is timed as K launches back to back (timed_batch); the
+        # grad-sync call, which waits on the host for its report, per call
+        batch = timed_batch(torch, once, K, warm=0) if c != "grad_sync" else None
     finally:
         rcc.finish(h)
     peak, src = peak_hbm()
     med = statistics.median(ms)
+    t = batch if batch is not None else med
     print(json.dumps({"case": c, "ranks": Rk, "elems": n, "dtype": args.dtype, "op": args.op,
                       "mode": "fast" if args.fast else "deterministic",
                       **({"gs_mode": args.gs_mode} if c == "grad_sync" else {}),
+                      "ms": round(t, 5),
+                      "timing": ("%d launches back to back between one event pair" % K
+                                 if batch is not None else
+                                 "median of %d calls, an event between calls" % K),
                       "median_ms": round(med, 5), "min_ms": round(min(ms), 5),
-                      "algbw_gbs": round(Rk * n * es / (med * 1e-3) / 1e9, 1),
-                      "traffic_gbs": round(traffic / (med * 1e-3) / 1e9, 1),
-                      "frac_of_" + src: round(traffic / (med * 1e-3) / 1e9 / peak, 4),
+                      "algbw_gbs": round(Rk * n * es / (t * 1e-3) / 1e9, 1),
+                      "traffic_gbs": round(traffic / (t * 1e-3) / 1e9, 1),
+                      "frac_of_" + src: round(traffic / (t * 1e-3) / 1e9 / peak, 4),
                       "min_traffic_bytes": traffic}), flush=True)
 
 
 def bench_sweep(args):
-    """The size sweep of the collectives (one process, CUDA-event timing, median)."""
+    """The size sweep of the collectives (one process; each point the mean of
+    back-to-back launches between one CUDA-event pair)."""
     import torch
     from gradient_sync_rcc_gb300 import build, rcc, synth
     build.build()
@@ -947,22 +1032,13 @@ def bench_sweep(args):
                         fn = lambda: rcc.reduce(h, ins, outs[Rk - 1], root=Rk - 1, op="mean")
                         traffic = (Rk + 1) * n * es
                     reps = 50 if traffic < (1 << 30) else 10
-                    for _ in range(3):
-                        fn()
-                    torch.cuda.synchronize()
-                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-                    ev[0].record()
-                    for k in range(reps):
-                        fn()
-                        ev[k + 1].record()
-                    torch.cuda.synchronize()
-                    ms = statistics.median(ev[k].elapsed_time(ev[k + 1]) for k in range(reps))
+                    ms = timed_batch(torch, fn, reps)
                 finally:
                     rcc.finish(h)
                 gbs = traffic / (ms * 1e-3) / 1e9
                 print(json.dumps({"sweep": case, "ranks": Rk, "elems": n,
                                   "dtype": "f32" if dt == rcc.F32 else "bf16",
-                                  "median_ms": round(ms, 5),
+                                  "ms": round(ms, 5), "timing": "%d back to back" % reps,
                                   "algbw_gbs": round(Rk * n * es / (ms * 1e-3) / 1e9, 1),
                                   "traffic_gbs": round(gbs, 1),
                                   "frac_of_" + src: round(gbs / peak, 4),

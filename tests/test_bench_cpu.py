@@ -58,8 +58,7 @@ def test_clock_sampler_keeps_only_the_timed_window(tmp_path, monkeypatch):
     fake.write_text("#!/bin/sh\n"
                     "i=0\n"
                     "while true; do\n"
-                    "  echo \"$((1000+i)), 2070, 0x0, Not Active, Not Active, Not Active, "
-                    "Not Active\"\n"
+                    "  echo \"$((1000+i)), 2070, 0x0000000000000000\"\n"
                     "  i=$((i+1)); sleep 0.05\n"
                     "done\n")
     fake.chmod(fake.stat().st_mode | stat.S_IEXEC)
@@ -78,3 +77,30 @@ def test_clock_sampler_keeps_only_the_timed_window(tmp_path, monkeypatch):
     assert c["window"] == "timed region" and c["samples"] >= 2
     assert c["sm_mhz"] >= 1000 + first        # none of the pre-roll samples counted
     assert c["sm_max_mhz"] == 2070 and c["reasons"] == []
+
+
+def test_clock_sampler_decodes_the_reasons_bitmask(tmp_path):
+    """NVML's clocks-event reason bits: 0x4 software power cap, 0x8 hardware
+    slowdown, 0x20 software thermal, 0x40 hardware thermal, 0x80 power brake;
+    the idle bit (0x1) is not a throttle reason."""
+    sys.path.insert(0, ROOT)
+    import bench
+    s = bench.ClockSampler(0)
+    s.f = open(tmp_path / "samples.csv", "w+")
+    s.f.write("2070, 2070, 0x0000000000000001\n"
+              "2055, 2070, 0x0000000000000004\n"
+              "1800, 2070, 0x00000000000000E8\n")
+    s.f.flush()
+
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            pass
+
+    s.proc = Done()
+    c = s.stop(0)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2055.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["hw_power_brake_slowdown", "hw_slowdown", "hw_thermal_slowdown",
+                            "sw_power_cap", "sw_thermal_slowdown"]
