@@ -691,9 +691,15 @@ cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   return launch_kernel(fn, dim3(gx, (unsigned)nseg), dim3(kThreads), 0, stream, a);
 }
 
+// A runtime source count (NS == 0, more than 8 ranks) always takes 16-byte
+// vectors: with 32-byte ones its 8-source groups need about 100 registers (2
+// CTAs per SM), and at 9-64 ranks reduce and reduce_scatter measured 0.88-1.01
+// of the copy peak against 0.91-1.10 with 16-byte vectors (all_reduce alike).
 template <typename T, int NS, int RED, bool FAST>
 cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  if (a.vec_ok >= 32 && vec_cap() >= 32) return launch_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+  if constexpr (NS > 0) {
+    if (a.vec_ok >= 32 && vec_cap() >= 32) return launch_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+  }
   return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
 }
 
@@ -717,11 +723,15 @@ cudaError_t launch_staged_reduce_w(int nseg, const MultiPtrArgs& a, cudaStream_t
 
 // bf16 takes 16-byte vectors here: with 32-byte ones a thread reduces and
 // stages twice the elements per vector, and the pass measured 0.72 of the
-// copy peak against 0.87 (8 ranks, odd shards).
+// copy peak against 0.87 (8 ranks, odd shards).  So does a runtime source
+// count: with 32-byte vectors the kernel needs 107 registers (2 CTAs per SM),
+// and a 12-rank reduce_scatter with odd shards measured 0.60 against 0.88.
 template <typename T, int NS, int RED, bool FAST>
 cudaError_t launch_staged_reduce_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  if (Elem<T>::kBytes == 4 && a.vec_ok >= 32 && vec_cap() >= 32)
-    return launch_staged_reduce_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+  if constexpr (NS > 0 && Elem<T>::kBytes == 4) {
+    if (a.vec_ok >= 32 && vec_cap() >= 32)
+      return launch_staged_reduce_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+  }
   return launch_staged_reduce_w<T, NS, RED, FAST, 4>(nseg, a, stream);
 }
 
