@@ -14,8 +14,9 @@ that batch:
 Metric (value): all_reduce algorithm GB/s = 3 * R*N*bytes / (time of the
 step's three all_reduce rows), those rows launched K times back to back
 between one CUDA-event pair.  The whole step (K steps of all eight rows, also
-back to back) is reported beside it (ms_per_step, step_algbw_gbs); a separate
-pass with an event between rows gives the per-row breakdown (rows).
+back to back) is reported beside it (ms_per_step, step_algbw_gbs), and so is
+the grad-sync row alone, K calls back to back (grad_sync_row); a separate pass
+with an event between rows gives the per-row breakdown (rows).
 Every input (512 MiB per row) exceeds the 129 MB L2, so no flush is needed.
 
 After the timed step the same line carries, each timed on its own:
@@ -310,6 +311,10 @@ class Workload:
         mark(8)
         return rep
 
+    def grad_sync_row(self, h):
+        """The step's grad-sync row alone."""
+        return self.rcc.grad_sync_adamw(h, self.sets, self.cfg, self.state)
+
     def ar_rows(self, h):
         """The metric's rows alone: the step's three all_reduce rows."""
         rcc = self.rcc
@@ -520,6 +525,8 @@ def bench_ours(args):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ar_start = torch.cuda.Event(enable_timing=True)
         ar_end = torch.cuda.Event(enable_timing=True)
+        gs_start = torch.cuda.Event(enable_timing=True)
+        gs_end = torch.cuda.Event(enable_timing=True)
         # load pre-roll: keep stepping (untimed) until the clock sampler is up
         # and has run 1.5 s
         t_pre = time.perf_counter()
@@ -551,9 +558,20 @@ def bench_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         launches2 = rcc.launch_count()
+        # timed region 3: the grad-sync row, K calls back to back
+        barrier(world)
+        torch.cuda.synchronize()
+        gs_start.record()
+        for k in range(K):
+            wl.grad_sync_row(h)
+        gs_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        launches3 = rcc.launch_count()
         clocks = sampler.stop(first_line)
         ms_total = start.elapsed_time(end)
         ar_ms_sum = ar_start.elapsed_time(ar_end) / K      # the three rows, per iteration
+        gs_ms = gs_start.elapsed_time(gs_end) / K
         # per-row breakdown (not a headline figure): Kr more steps with an event
         # between rows, which adds about 2-4 us of device time to each row
         for k in range(Kr):
@@ -591,6 +609,7 @@ def bench_ours(args):
     max_step, total_step = combine_ranks(ms_step, alg_step, world, device)
     max_e2e, total_e2e = combine_ranks(e2e_ar_ms, ALG_BYTES_ROW * len(ar_rows), world, device)
     max_e2e_step, total_e2e_step = combine_ranks(e2e_ms, alg_step, world, device)
+    max_gs, _ = combine_ranks(gs_ms, 0, world, device)
     if rank != 0:
         return
     peak, peak_src = peak_hbm()
@@ -623,8 +642,9 @@ def bench_ours(args):
                    "adamw_replicas": 1, "l2": "inputs 512 MiB per row > 129 MB L2, no flush",
                    "timing": ("value: K iterations of the three all_reduce rows launched back "
                               "to back between one CUDA-event pair; ms_per_step: K steps of "
-                              "all eight rows likewise; rows: a separate pass of min(K, 20) "
-                              "steps with an event between rows (each row about 2-4 us more)"),
+                              "all eight rows likewise; grad_sync_row: K grad-sync calls "
+                              "likewise; rows: a separate pass of min(K, 20) steps with an "
+                              "event between rows (each row about 2-4 us more)"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_algbw_gbs": round(total_step / (max_step * 1e-3) / 1e9, 2),
         "roofline": {"kernel": "all_reduce (multi-pointer pass, fp32, R=8, N=2^24)",
@@ -638,6 +658,13 @@ def bench_ours(args):
                      "algorithmic_bytes_per_launch": ar_traffic,
                      "avg_launch_ms": round(ar_ms, 4)},
         "rows": rows,
+        "grad_sync_row": {"ms": round(max_gs, 4),
+                          "traffic_gbs": round(MIN_TRAFFIC["grad_sync_adamw"] / (max_gs * 1e-3) / 1e9, 1),
+                          "frac_of_" + peak_src: round(MIN_TRAFFIC["grad_sync_adamw"] / (max_gs * 1e-3)
+                                                       / 1e9 / peak, 4),
+                          "min_traffic_bytes": MIN_TRAFFIC["grad_sync_adamw"],
+                          "timing": "the step's grad-sync row alone, K calls back to back "
+                                    "between one event pair (each call reads its report back)"},
         "e2e": {"value": round(total_e2e / (max_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(max_e2e, 3),
                 "what": "per step: the 8 rank inputs copied from pinned host memory, the "
@@ -649,9 +676,10 @@ def bench_ours(args):
                      "ms_per_step": round(max_e2e_step, 3),
                      "what": "the whole step (all eight rows) with host inputs, as e2e",
                      "h2d_bytes_per_step": R * N * ES, "d2h_bytes_per_step": N * ES + 12},
-        "gpu_launches": int(launches2 - launches0),
+        "gpu_launches": int(launches3 - launches0),
         "gpu_launches_per_region": {"step": int(launches1 - launches0),
-                                    "value": int(launches2 - launches1)},
+                                    "value": int(launches2 - launches1),
+                                    "grad_sync_row": int(launches3 - launches2)},
         "clocks": clocks,
         "d2d_copy_gbs_measured_here": round(copy_gbs, 1),
     }
