@@ -82,7 +82,8 @@ def parse_args():
                     help="leave out the bf16 RS/AG and 1024-tensor grad-sync legs of the line")
     ap.add_argument("--case", default="step",
                     choices=["step", "all_reduce", "reduce", "broadcast", "reduce_scatter",
-                             "all_gather", "all_to_all", "grad_sync", "grad_sync_1024"],
+                             "all_gather", "all_to_all", "grad_sync", "grad_sync_1024",
+                             "all_reduce_rank"],
                     help="step: the whole hot path (the benchmark line); otherwise time one "
                          "collective alone on --ranks x --elems (profiling and sweeps)")
     ap.add_argument("--ranks", type=int, default=R)
@@ -1031,6 +1032,79 @@ def bench_case(args):
                       "min_traffic_bytes": traffic}), flush=True)
 
 
+def bench_rank_case(args):
+    """all_reduce through the per-rank arrival API: one host thread and one
+    CUDA stream per rank, each calling rcc_all_reduce_rank with its own
+    buffers; the last rank to arrive launches the kernel, which waits for every
+    rank's stream, and every rank's stream waits for it.  K rounds; the device
+    time per round is taken on rank 0's stream between one event pair, the
+    host time per round over all threads.  A second pass at 1,024 elements per
+    rank gives the arrival protocol's own cost per round (host-bound)."""
+    import threading
+    import torch
+    from gradient_sync_rcc_gb300 import build, rcc, synth
+    build.build()
+    dev = "cuda:0"
+    Rk, K = args.ranks, args.steps
+    peak, src = peak_hbm()
+
+    def rounds(n, K):
+        ins = synth.gpu_rank_buffers("uniform", Rk, n, torch.float32, (7, Rk, n), dev)
+        outs = [torch.empty(n, device=dev) for _ in range(Rk)]
+        streams = [torch.cuda.Stream() for _ in range(Rk)]
+        h = rcc.register(0, Rk, rcc.F32, not args.fast)
+        errs = []
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gate = threading.Barrier(Rk)
+
+        def rank(r, nround, timed):
+            try:
+                s = streams[r]
+                gate.wait()
+                if timed and r == 0:
+                    start.record(s)
+                for _ in range(nround):
+                    rcc.all_reduce_rank(h, r, ins[r], outs[r], args.op, stream=s)
+                if timed and r == 0:
+                    end.record(s)
+            except BaseException as e:  # reported below
+                errs.append(e)
+
+        def run(nround, timed):
+            ts = [threading.Thread(target=rank, args=(r, nround, timed)) for r in range(Rk)]
+            t0 = time.perf_counter()
+            for t in ts:
+                t.start()
+            for t in ts:
+                t.join()
+            torch.cuda.synchronize()
+            return time.perf_counter() - t0
+
+        try:
+            torch.cuda.synchronize()
+            run(3, False)                       # warm-up rounds
+            wall = run(K, True)
+        finally:
+            rcc.finish(h)
+        if errs:
+            raise errs[0]
+        return start.elapsed_time(end) / K, wall * 1e3 / K
+
+    dev_ms, host_ms = rounds(args.elems, K)
+    _, small_host_ms = rounds(1024, max(K, 200))
+    traffic = 2 * Rk * args.elems * 4
+    print(json.dumps({"case": "all_reduce_rank", "ranks": Rk, "elems": args.elems, "dtype": "f32",
+                      "op": args.op, "mode": "fast" if args.fast else "deterministic",
+                      "rounds": K, "ms": round(dev_ms, 5),
+                      "timing": "rank 0's stream, K rounds between one event pair",
+                      "host_ms_per_round": round(host_ms, 4),
+                      "arrival_us_per_round_1024_elems": round(small_host_ms * 1e3, 1),
+                      "algbw_gbs": round(Rk * args.elems * 4 / (dev_ms * 1e-3) / 1e9, 1),
+                      "traffic_gbs": round(traffic / (dev_ms * 1e-3) / 1e9, 1),
+                      "frac_of_" + src: round(traffic / (dev_ms * 1e-3) / 1e9 / peak, 4),
+                      "min_traffic_bytes": traffic}), flush=True)
+
+
 def bench_sweep(args):
     """The size sweep of the collectives (one process; each point the mean of
     back-to-back launches between one CUDA-event pair)."""
@@ -1082,6 +1156,9 @@ def main():
         return
     if args.case == "grad_sync_1024":
         bench_grad_sync_1024(args)
+        return
+    if args.case == "all_reduce_rank":
+        bench_rank_case(args)
         return
     if args.case != "step":
         bench_case(args)
