@@ -288,9 +288,9 @@ struct SegView {
 
 // NS > 0: compile-time number of sources (U vectors per thread in flight per
 // source); NS == 0: runtime count (any R up to kMaxRanks), sources loaded in
-// groups of 8 and folded in rank order.  W: 32-bit words per vector (4 or 8);
+// groups of G and folded in rank order.  W: 32-bit words per vector (4 or 8);
 // the host picks 8 only when every address is 32-byte aligned.
-template <typename T, int NS, int RED, bool FAST, int U, int W>
+template <typename T, int NS, int RED, bool FAST, int U, int W, int G = 8>
 __global__ void RCC_BOUNDS mp_kernel(const __grid_constant__ MultiPtrArgs a) {
   pdl_wait_then_release();
   using E = Elem<T>;
@@ -363,18 +363,19 @@ __global__ void RCC_BOUNDS mp_kernel(const __grid_constant__ MultiPtrArgs a) {
       }
     }
   } else {
-    // runtime rank count: rank order fold in groups of 8 sources
+    // runtime rank count: rank order fold in groups of G sources, each
+    // group's loads all issued before any of it is folded
     const int R = a.nsrc;
     for (size_t idx = tid; idx < nv; idx += nthreads) {
       Acc<RED> acc[EPV];
-      for (int q0 = 0; q0 < R; q0 += 8) {
-        Vec<W> v[8];
+      for (int q0 = 0; q0 < R; q0 += G) {
+        Vec<W> v[G];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < G; ++k)
           if (q0 + k < R)
             v[k] = ld_vec<W>(static_cast<const char*>(sv.src(q0 + k, EB)) + idx * VB);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < G; ++k) {
           if (q0 + k < R) {
             float f[EPV];
             E::template unpack<W>(v[k], f);
@@ -672,12 +673,12 @@ inline int vec_cap() {
   return cap;
 }
 
-template <typename T, int NS, int RED, bool FAST, int W>
+template <typename T, int NS, int RED, bool FAST, int W, int G = 8>
 cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   constexpr int U0 = NS > 0 ? unroll_for(NS, RED) * 4 / W : 1;
   constexpr int U = U0 > 0 ? U0 : 1;
   constexpr int EPV = W * Elem<T>::kPerWord;
-  auto fn = mp_kernel<T, NS, RED, FAST, U, W>;
+  auto fn = mp_kernel<T, NS, RED, FAST, U, W, G>;
   const size_t nv = a.vec_ok >= 4 * W ? a.n / EPV : 0;
   const size_t tail = a.n - nv * EPV;
   size_t want = (nv + (size_t)kThreads * U - 1) / ((size_t)kThreads * U);
@@ -695,12 +696,19 @@ cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
 // vectors: with 32-byte ones its 8-source groups need about 100 registers (2
 // CTAs per SM), and at 9-64 ranks reduce and reduce_scatter measured 0.88-1.01
 // of the copy peak against 0.91-1.10 with 16-byte vectors (all_reduce alike).
+// 9-12 sources load as one group of 12 (one load round trip instead of two:
+// reduce and reduce_scatter at 9 ranks 0.93 / 0.91 -> 1.01 / 1.01); other
+// counts in groups of 8 (a group of 12 or 16 holds too many registers for
+// the occupancy that 16 ranks and up want: 1.09 -> 0.98 at 16).
 template <typename T, int NS, int RED, bool FAST>
 cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   if constexpr (NS > 0) {
     if (a.vec_ok >= 32 && vec_cap() >= 32) return launch_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+    return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
+  } else {
+    if (a.nsrc <= 12) return launch_w<T, 0, RED, FAST, 4, 12>(nseg, a, stream);
+    return launch_w<T, 0, RED, FAST, 4, 8>(nseg, a, stream);
   }
-  return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
 }
 
 // grid for the staged kernels: one CTA per tile up to RCC_WAVES waves
