@@ -430,10 +430,14 @@ __global__ void RCC_BOUNDS mp_kernel(const __grid_constant__ MultiPtrArgs a) {
 // global access stays coalesced:
 //   staged_reduce_kernel  sources aligned (reduce_scatter: R reads per write):
 //                         vector loads, reduce, tile to shared memory, then
-//                         4- or 2-byte stores in consecutive order;
-//   staged_copy_kernel    destinations aligned (all_gather, all_to_all): loads
-//                         in consecutive order into shared memory, then vector
-//                         stores to every destination.
+//                         vector stores from each destination's first vector
+//                         boundary in the tile (element stores at its ends);
+//   staged_copy_kernel    destinations aligned (all_gather, all_to_all): vector
+//                         loads from the source's vector boundary at or below
+//                         the tile into shared memory, then vector stores to
+//                         every destination read back at the source's shift.
+// Either way both global sides move whole vectors; the shift between them is
+// taken in shared memory.
 // kStageU vectors per thread per tile.
 constexpr int kStageU = 2;
 
@@ -465,29 +469,92 @@ __device__ __forceinline__ void scalar_range(const MultiPtrArgs& a, const SegVie
   }
 }
 
-// Raw element bits (fp32: 4 bytes, bf16: 2 bytes) at index i.
+// The staged kernels' tile in shared memory, word-major: word j of vector v
+// at words[j][v].  A thread that writes its whole vector, or reads back the W
+// words that start at any element offset, then touches consecutive banks
+// across the warp.
+template <int W>
+struct StageTile {
+  static constexpr int kVecs = kThreads * kStageU + 1;  // one spare for a shifted window
+  uint32_t words[W][kVecs];
+
+  __device__ __forceinline__ void put(int v, const Vec<W>& x) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) words[k][v] = x.w[k];
+  }
+  __device__ __forceinline__ uint32_t word(int p) const { return words[p % W][p / W]; }
+  // The vector of EPV elements that starts at tile element `off` (EB-byte
+  // elements; a 2-byte element at an odd offset straddles two words).
+  template <int EB>
+  __device__ __forceinline__ Vec<W> get(int off) const {
+    Vec<W> x;
+    if constexpr (EB == 4) {
+#pragma unroll
+      for (int k = 0; k < W; ++k) x.w[k] = word(off + k);
+    } else {
+      const int p = off >> 1;
+      if ((off & 1) == 0) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) x.w[k] = word(p + k);
+      } else {
+        uint32_t lo = word(p);
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const uint32_t hi = word(p + k + 1);
+          x.w[k] = __funnelshift_r(lo, hi, 16);
+          lo = hi;
+        }
+      }
+    }
+    return x;
+  }
+  // One element's raw bits at tile element `e`.
+  template <int EB>
+  __device__ __forceinline__ uint32_t elem(int e) const {
+    if constexpr (EB == 4) {
+      return word(e);
+    } else {
+      return (word(e >> 1) >> (16 * (e & 1))) & 0xFFFFu;
+    }
+  }
+};
+
+// Stores raw element bits b (EB bytes) at element index i of p.
 template <int EB>
-struct Raw;
-template <>
-struct Raw<4> {
-  using type = uint32_t;
-};
-template <>
-struct Raw<2> {
-  using type = uint16_t;
-};
+__device__ __forceinline__ void put_elem(void* p, size_t i, uint32_t b) {
+  if constexpr (EB == 4) {
+    static_cast<uint32_t*>(p)[i] = b;
+  } else {
+    static_cast<uint16_t*>(p)[i] = (uint16_t)b;
+  }
+}
+
+template <int EB>
+__device__ __forceinline__ uint32_t get_elem(const void* p, size_t i) {
+  if constexpr (EB == 4) {
+    return static_cast<const uint32_t*>(p)[i];
+  } else {
+    return static_cast<const uint16_t*>(p)[i];
+  }
+}
+
+// Element offset of address p from the VB-byte boundary below it.
+template <int VB, int EB>
+__device__ __forceinline__ int vec_phase(const void* p) {
+  return (int)((reinterpret_cast<uintptr_t>(p) % VB) / EB);
+}
 
 template <typename T, int NS, int RED, bool FAST, int W>
 __global__ void __launch_bounds__(kThreads)
     staged_reduce_kernel(const __grid_constant__ MultiPtrArgs a) {
   pdl_wait_then_release();
   using E = Elem<T>;
-  using B = typename Raw<E::kBytes>::type;
   constexpr int EPV = W * E::kPerWord;
   constexpr int VB = 4 * W;
   constexpr int EB = E::kBytes;
-  constexpr int TILE = kThreads * kStageU * EPV;
-  __shared__ Vec<W> tile[kThreads * kStageU];
+  constexpr int NV = kThreads * kStageU;
+  constexpr int TILE = NV * EPV;
+  __shared__ StageTile<W> tile;
   const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
                    (size_t)blockIdx.y * a.dst_seg_stride};
   const int ndst = sv.ndst();
@@ -546,35 +613,24 @@ __global__ void __launch_bounds__(kThreads)
         for (int e = 0; e < EPV; ++e) r[e] = acc[e].result(a.mean_div);
         out = E::template pack<W>(r);
       }
-      tile[slot] = out;
+      tile.put(slot, out);
     }
     __syncthreads();
-    const B* bits = reinterpret_cast<const B*>(tile);
-    if constexpr (EB == 2) {
-      // 2-byte elements leave the tile as 4-byte words: pairs start at the
-      // first element on a 4-byte boundary of the (common) destination offset
-      const int shift = (int)((reinterpret_cast<uintptr_t>(sv.dst(0, EB)) / 2 + e0) & 1);
-#pragma unroll
-      for (int k = 0; k < kStageU * EPV / 2; ++k) {
-        const int j = 2 * (k * kThreads + threadIdx.x) + shift;
-        if (j + 1 < TILE) {
-          const uint32_t w = (uint32_t)bits[j] | ((uint32_t)bits[j + 1] << 16);
-          for (int d = 0; d < ndst; ++d)
-            *reinterpret_cast<uint32_t*>(static_cast<B*>(sv.dst(d, EB)) + e0 + j) = w;
-        }
+    // Each destination gets vector stores from its first VB boundary in the
+    // tile on (read from the tile at that shift), and element stores for the
+    // partial vectors at the tile's two ends.
+    for (int d = 0; d < ndst; ++d) {
+      char* dst = static_cast<char*>(sv.dst(d, EB));
+      const int lead = (EPV - vec_phase<VB, EB>(dst + e0 * EB)) % EPV;
+      const int nvec = (TILE - lead) / EPV;
+      for (int k = threadIdx.x; k < nvec; k += kThreads) {
+        const int off = lead + k * EPV;
+        st_vec<W>(dst + (e0 + off) * EB, tile.template get<EB>(off));
       }
-      if (shift && threadIdx.x == 0) {  // the two elements outside the pairs
-        for (int d = 0; d < ndst; ++d) {
-          static_cast<B*>(sv.dst(d, EB))[e0] = bits[0];
-          static_cast<B*>(sv.dst(d, EB))[e0 + TILE - 1] = bits[TILE - 1];
-        }
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < kStageU * EPV; ++k) {
-        const int idx = k * kThreads + threadIdx.x;
-        const B b = bits[idx];
-        for (int d = 0; d < ndst; ++d) static_cast<B*>(sv.dst(d, EB))[e0 + idx] = b;
+      const int tail0 = lead + nvec * EPV;
+      for (int e = threadIdx.x; e < lead + (TILE - tail0); e += kThreads) {
+        const int te = e < lead ? e : tail0 + (e - lead);
+        put_elem<EB>(dst, e0 + te, tile.template elem<EB>(te));
       }
     }
     __syncthreads();
@@ -589,35 +645,61 @@ template <typename T, int W>
 __global__ void __launch_bounds__(kThreads) staged_copy_kernel(const __grid_constant__ MultiPtrArgs a) {
   pdl_wait_then_release();
   using E = Elem<T>;
-  using B = typename Raw<E::kBytes>::type;
   constexpr int EPV = W * E::kPerWord;
   constexpr int VB = 4 * W;
   constexpr int EB = E::kBytes;
-  constexpr int TILE = kThreads * kStageU * EPV;
-  __shared__ Vec<W> tile[kThreads * kStageU];
+  constexpr int NV = kThreads * kStageU;
+  constexpr int TILE = NV * EPV;
+  __shared__ StageTile<W> tile;
   const SegView sv{a, (int)blockIdx.y, (size_t)blockIdx.y * a.src_seg_stride,
                    (size_t)blockIdx.y * a.dst_seg_stride};
   const int ndst = sv.ndst();
-  const B* src = static_cast<const B*>(sv.src(0, EB));
+  const char* src = static_cast<const char*>(sv.src(0, EB));
   // every destination of the segment has the same offset from a VB-aligned base
   const uintptr_t anchor = reinterpret_cast<uintptr_t>(sv.dst(0, EB));
   size_t head = ((VB - anchor % VB) % VB) / EB;
   if (head > a.n) head = a.n;
   const size_t ntiles = (a.n - head) / TILE;
-  B* bits = reinterpret_cast<B*>(tile);
   for (size_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const size_t e0 = head + t * TILE;
-    B v[kStageU * EPV];
+    // source vectors from the VB boundary at or below element e0 (`lag`
+    // elements before it) until the tile is covered; a vector that reaches
+    // outside the segment is read element by element
+    const int lag = vec_phase<VB, EB>(src + e0 * EB);
+    const int nsv = NV + (lag ? 1 : 0);
+    // every load of the thread is issued before any is written to the tile
+    Vec<W> x[kStageU + 1];
 #pragma unroll
-    for (int k = 0; k < kStageU * EPV; ++k) v[k] = src[e0 + k * kThreads + threadIdx.x];
+    for (int u = 0; u <= kStageU; ++u) {
+      const int j = u * kThreads + threadIdx.x;
+      if (j >= nsv) continue;
+      const long long s0 = (long long)e0 - lag + (long long)j * EPV;
+      if (s0 >= 0 && s0 + EPV <= (long long)a.n) {
+        x[u] = ld_vec<W>(src + s0 * EB);
+      } else {
 #pragma unroll
-    for (int k = 0; k < kStageU * EPV; ++k) bits[k * kThreads + threadIdx.x] = v[k];
+        for (int k = 0; k < W; ++k) x[u].w[k] = 0u;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const long long i = s0 + e;
+          if (i >= 0 && i < (long long)a.n) {
+            const uint32_t b = get_elem<EB>(src, (size_t)i);
+            x[u].w[e * EB / 4] |= b << (8 * ((e * EB) % 4));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u <= kStageU; ++u) {
+      const int j = u * kThreads + threadIdx.x;
+      if (j < nsv) tile.put(j, x[u]);
+    }
     __syncthreads();
 #pragma unroll
     for (int u = 0; u < kStageU; ++u) {
-      const int slot = u * kThreads + threadIdx.x;
-      const Vec<W> out = tile[slot];
-      const size_t off = (e0 + (size_t)slot * EPV) * EB;
+      const int k = u * kThreads + threadIdx.x;
+      const Vec<W> out = tile.template get<EB>(lag + k * EPV);
+      const size_t off = (e0 + (size_t)k * EPV) * EB;
       for (int d = 0; d < ndst; ++d) st_vec<W>(static_cast<char*>(sv.dst(d, EB)) + off, out);
     }
     __syncthreads();
