@@ -483,27 +483,38 @@ struct StageTile {
     for (int k = 0; k < W; ++k) words[k][v] = x.w[k];
   }
   __device__ __forceinline__ uint32_t word(int p) const { return words[p % W][p / W]; }
-  // The vector of EPV elements that starts at tile element `off` (EB-byte
-  // elements; a 2-byte element at an odd offset straddles two words).
+
+  // Reads of whole vectors at one element shift `sh` (the same for every
+  // vector of a segment): the vector that starts at tile element sh + v*EPV
+  // takes words v*W + ph + i (i = 0..W, ph the shift in words), which sit at
+  // words[(ph + i) % W][v + (ph + i) / W].  The W + 1 word offsets are worked
+  // out once; each read is then one add and one shared load per word.
+  struct Shift {
+    int at[W + 1];  // byte offset of word i for vector 0
+    bool odd;       // a 2-byte element shift of one half word: funnel shifts
+  };
   template <int EB>
-  __device__ __forceinline__ Vec<W> get(int off) const {
+  __device__ __forceinline__ static Shift shift(int sh) {
+    Shift f;
+    const int ph = EB == 4 ? sh : sh >> 1;
+    f.odd = EB == 2 && (sh & 1);
+#pragma unroll
+    for (int i = 0; i <= W; ++i) f.at[i] = (((ph + i) % W) * kVecs + (ph + i) / W) * 4;
+    return f;
+  }
+  __device__ __forceinline__ Vec<W> get(int v, const Shift& f) const {
+    const char* base = reinterpret_cast<const char*>(&words[0][0]) + v * 4;
     Vec<W> x;
-    if constexpr (EB == 4) {
+    if (!f.odd) {
 #pragma unroll
-      for (int k = 0; k < W; ++k) x.w[k] = word(off + k);
+      for (int k = 0; k < W; ++k) x.w[k] = *reinterpret_cast<const uint32_t*>(base + f.at[k]);
     } else {
-      const int p = off >> 1;
-      if ((off & 1) == 0) {
+      uint32_t lo = *reinterpret_cast<const uint32_t*>(base + f.at[0]);
 #pragma unroll
-        for (int k = 0; k < W; ++k) x.w[k] = word(p + k);
-      } else {
-        uint32_t lo = word(p);
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const uint32_t hi = word(p + k + 1);
-          x.w[k] = __funnelshift_r(lo, hi, 16);
-          lo = hi;
-        }
+      for (int k = 0; k < W; ++k) {
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(base + f.at[k + 1]);
+        x.w[k] = __funnelshift_r(lo, hi, 16);
+        lo = hi;
       }
     }
     return x;
@@ -623,10 +634,9 @@ __global__ void __launch_bounds__(kThreads)
       char* dst = static_cast<char*>(sv.dst(d, EB));
       const int lead = (EPV - vec_phase<VB, EB>(dst + e0 * EB)) % EPV;
       const int nvec = (TILE - lead) / EPV;
-      for (int k = threadIdx.x; k < nvec; k += kThreads) {
-        const int off = lead + k * EPV;
-        st_vec<W>(dst + (e0 + off) * EB, tile.template get<EB>(off));
-      }
+      const auto sh = StageTile<W>::template shift<EB>(lead);
+      for (int k = threadIdx.x; k < nvec; k += kThreads)
+        st_vec<W>(dst + (e0 + lead + (size_t)k * EPV) * EB, tile.get(k, sh));
       const int tail0 = lead + nvec * EPV;
       for (int e = threadIdx.x; e < lead + (TILE - tail0); e += kThreads) {
         const int te = e < lead ? e : tail0 + (e - lead);
@@ -695,10 +705,11 @@ __global__ void __launch_bounds__(kThreads) staged_copy_kernel(const __grid_cons
       if (j < nsv) tile.put(j, x[u]);
     }
     __syncthreads();
+    const auto sh = StageTile<W>::template shift<EB>(lag);
 #pragma unroll
     for (int u = 0; u < kStageU; ++u) {
       const int k = u * kThreads + threadIdx.x;
-      const Vec<W> out = tile.template get<EB>(lag + k * EPV);
+      const Vec<W> out = tile.get(k, sh);
       const size_t off = (e0 + (size_t)k * EPV) * EB;
       for (int d = 0; d < ndst; ++d) st_vec<W>(static_cast<char*>(sv.dst(d, EB)) + off, out);
     }

@@ -74,15 +74,26 @@ def run(kThreads, kStageU, W, EB, n, src_mis, dst_mis, kind, nblocks=3):
             x = words[p % W][p // W]
             assert x is not None, ("smem read of unwritten word", p)
             return x
-        def get(off):
-            if EB == 4:
-                return [word(off + k) for k in range(W)]
-            p = off >> 1
-            if off % 2 == 0:
-                return [word(p + k) for k in range(W)]
-            lo = word(p); r = []
+        def shift(sh):
+            # the kernels' StageTile::shift: byte offsets of the W + 1 words
+            # that vector 0 reads at element shift sh, and the half-word flag
+            ph = sh if EB == 4 else sh >> 1
+            at = [(((ph + i) % W) * KV + (ph + i) // W) * 4 for i in range(W + 1)]
+            return at, (EB == 2 and sh % 2 == 1)
+        def word_at(byte_off):
+            j, v = divmod(byte_off // 4, KV)
+            assert 0 <= j < W and 0 <= v < KV, ("smem read outside", byte_off)
+            x = words[j][v]
+            assert x is not None, ("smem read of unwritten word", byte_off)
+            return x
+        def get_v(v, f):
+            at, odd = f
+            base = v * 4
+            if not odd:
+                return [word_at(base + at[k]) for k in range(W)]
+            lo = word_at(base + at[0]); r = []
             for k in range(W):
-                hi = word(p + k + 1)
+                hi = word_at(base + at[k + 1])
                 r.append(((lo >> 16) | (hi << 16)) & 0xFFFFFFFF)
                 lo = hi
             return r
@@ -96,9 +107,10 @@ def run(kThreads, kStageU, W, EB, n, src_mis, dst_mis, kind, nblocks=3):
                 put(slot, to_words(el))
             lead = (EPV - phase(dst_base + e0 * EB)) % EPV
             nvec = (TILE - lead) // EPV
+            f = shift(lead)
             for k in range(nvec):
                 off = lead + k * EPV
-                store_vec(dst_base + (e0 + off) * EB, from_words(get(off)))
+                store_vec(dst_base + (e0 + off) * EB, from_words(get_v(k, f)))
             tail0 = lead + nvec * EPV
             for e in range(lead + (TILE - tail0)):
                 te = e if e < lead else tail0 + (e - lead)
@@ -113,8 +125,9 @@ def run(kThreads, kStageU, W, EB, n, src_mis, dst_mis, kind, nblocks=3):
                 else:
                     el = [load_elem(s0 + e) if 0 <= s0 + e < n else 0 for e in range(EPV)]
                 put(j, to_words(el))
+            f = shift(lag)
             for k in range(NV):
-                store_vec(dst_base + (e0 + k * EPV) * EB, from_words(get(lag + k * EPV)))
+                store_vec(dst_base + (e0 + k * EPV) * EB, from_words(get_v(k, f)))
     # scalar ranges
     for i in list(range(0, head)) + list(range(head + ntiles * TILE, n)):
         store_elem(i, load_elem(i))
