@@ -158,16 +158,38 @@ def launch_count():
 
 # ------------------------------------------------------------- marshalling
 
+_PTR_TYPES = {}
+_CONST_ARRAYS = {}
+
+
 def ptr_array(ptrs):
-    return (C.c_void_p * len(ptrs))(*[None if p is None or p == 0 else int(p) for p in ptrs])
+    """A void* array (None and 0 are NULL)."""
+    ty = _PTR_TYPES.get(len(ptrs))
+    if ty is None:
+        ty = _PTR_TYPES[len(ptrs)] = C.c_void_p * len(ptrs)
+    return ty(*ptrs)
+
+
+def _const_array(ctype, vals):
+    # count and op arrays repeat from call to call and the library only reads
+    # them: one array per distinct content (the table is cleared past 256)
+    key = (ctype, tuple(vals))
+    arr = _CONST_ARRAYS.get(key)
+    if arr is None:
+        if len(_CONST_ARRAYS) > 256:
+            _CONST_ARRAYS.clear()
+        arr = _CONST_ARRAYS[key] = (ctype * len(vals))(*vals)
+    return arr
 
 
 def size_array(vals):
-    return (C.c_size_t * len(vals))(*vals)
+    """A read-only size_t array for the library's count arguments."""
+    return _const_array(C.c_size_t, vals)
 
 
 def int_array(vals):
-    return (C.c_int * len(vals))(*vals)
+    """A read-only int array for the library's op and root arguments."""
+    return _const_array(C.c_int, vals)
 
 
 def _ptr(t):
