@@ -268,16 +268,23 @@ struct SegView {
   const MultiPtrArgs& a;
   int seg;
   size_t soff, doff;  // element offsets of this segment
+  int a2a_hi, a2a_lo;  // all-to-all: seg / R and seg % R, worked out once
+  __device__ __forceinline__ SegView(const MultiPtrArgs& a_, int seg_, size_t soff_, size_t doff_)
+      : a(a_), seg(seg_), soff(soff_), doff(doff_), a2a_hi(0), a2a_lo(0) {
+    if (a.a2a_ranks > 0) {
+      a2a_hi = seg / a.a2a_ranks;
+      a2a_lo = seg - a2a_hi * a.a2a_ranks;
+    }
+  }
   __device__ __forceinline__ const void* src(int q, int eb) const {
     if (a.a2a_ranks > 0)  // chunk (seg % R) of rank (seg / R)
-      return static_cast<const char*>(a.src[seg / a.a2a_ranks]) +
-             (size_t)(seg % a.a2a_ranks) * a.n * eb;
+      return static_cast<const char*>(a.src[a2a_hi]) + (size_t)a2a_lo * a.n * eb;
     const void* base = a.src_per_seg ? a.src[seg] : a.src[q];
     return static_cast<const char*>(base) + soff * eb;
   }
   __device__ __forceinline__ void* dst(int d, int eb) const {
     if (a.a2a_ranks > 0)  // slot (seg / R) of rank (seg % R)
-      return static_cast<char*>(a.dst[seg % a.a2a_ranks]) + (size_t)(seg / a.a2a_ranks) * a.n * eb;
+      return static_cast<char*>(a.dst[a2a_lo]) + (size_t)a2a_hi * a.n * eb;
     void* base = a.dst_per_seg ? a.dst[seg] : a.dst[d];
     return static_cast<char*>(base) + doff * eb;
   }
