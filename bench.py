@@ -183,10 +183,8 @@ def ncu_traffic():
 
 
 class ClockSampler:
-    # Only the reasons bitmask is queried: the first process on a fresh box that
-    # also queried the four per-reason fields saw the GPU stall 60-140 ms about
-    # a second into a timed region with no idle gaps.  The bits are NVML's
-    # clocks-event reasons.
+    # One query field holds every throttle reason: the reasons bitmask, whose
+    # bits are NVML's clocks-event reasons.
     FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
     REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
