@@ -454,3 +454,19 @@ def test_nvtx_ranges_do_not_change_behaviour():
     out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
                          env=dict(os.environ, RCC_NVTX="1"), timeout=120)
     assert out.returncode == 0 and "nvtx ok" in out.stdout, out.stdout + out.stderr
+
+
+def test_marshalling_arrays():
+    """The binding's argument arrays: pointer arrays map None and 0 to NULL;
+    count and op arrays, which the library only reads, are shared between
+    calls with the same contents and never between different contents."""
+    from gradient_sync_rcc_gb300 import rcc
+    p = rcc.ptr_array([0, None, 4096])
+    assert list(p) == [None, None, 4096]
+    a = rcc.size_array([8, 8, 7])
+    assert list(a) == [8, 8, 7]
+    assert rcc.size_array([8, 8, 7]) is a
+    assert list(rcc.size_array([8, 8, 8])) == [8, 8, 8]
+    assert rcc.int_array([8, 8, 7]) is not a and list(rcc.int_array([8, 8, 7])) == [8, 8, 7]
+    for k in range(300):                      # the table is cleared, contents stay right
+        assert list(rcc.size_array([k, k + 1])) == [k, k + 1]
