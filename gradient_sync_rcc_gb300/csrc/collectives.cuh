@@ -801,13 +801,15 @@ cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
 // reduce and reduce_scatter at 9 ranks 0.93 / 0.91 -> 1.01 / 1.01); other
 // counts in groups of 8 (a group of 12 or 16 holds too many registers for
 // the occupancy that 16 ranks and up want: 1.09 -> 0.98 at 16).
-// A copy whose default grid stays below the wave cap takes half the vectors
-// per thread: twice the CTAs, so the last partial wave is half as long.  At 8
-// ranks, broadcast and all_gather of 2^22 / 2^23 fp32 went from 0.77 / 0.91 to
-// 0.90 / 0.98 of the copy peak; at 2^26 (a capped grid) the default measured
-// 1.015 against 0.999, so capped grids keep it.
+// A launch with more than one vector per thread (copies, and reductions over
+// one or two sources) takes half as many when its default grid stays below
+// the wave cap: twice the CTAs, so the last partial wave is half as long.  At
+// 8 ranks, broadcast and all_gather of 2^22 / 2^23 fp32 went from 0.77 / 0.91
+// to 0.90 / 0.98 of the copy peak (two-rank reductions gained 0-4%); at 2^26
+// (a capped grid) the default measured 1.015 against 0.999, so capped grids
+// keep it.
 template <typename T, int NS, int RED, bool FAST, int W>
-cudaError_t launch_copy_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
+cudaError_t launch_unrolled_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   constexpr int U0 = unroll_for(NS, RED) * 4 / W;
   if constexpr (U0 > 1) {
     constexpr int EPV = W * Elem<T>::kPerWord;
@@ -822,12 +824,10 @@ cudaError_t launch_copy_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) 
 
 template <typename T, int NS, int RED, bool FAST>
 cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
-  if constexpr (NS > 0 && RED == kRedCopy) {
-    if (a.vec_ok >= 32 && vec_cap() >= 32) return launch_copy_w<T, NS, RED, FAST, 8>(nseg, a, stream);
-    if (a.vec_ok >= 16) return launch_copy_w<T, NS, RED, FAST, 4>(nseg, a, stream);
-    return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
-  } else if constexpr (NS > 0) {
-    if (a.vec_ok >= 32 && vec_cap() >= 32) return launch_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+  if constexpr (NS > 0) {
+    if (a.vec_ok >= 32 && vec_cap() >= 32)
+      return launch_unrolled_w<T, NS, RED, FAST, 8>(nseg, a, stream);
+    if (a.vec_ok >= 16) return launch_unrolled_w<T, NS, RED, FAST, 4>(nseg, a, stream);
     return launch_w<T, NS, RED, FAST, 4>(nseg, a, stream);
   } else {
     if (a.nsrc <= 12) return launch_w<T, 0, RED, FAST, 4, 12>(nseg, a, stream);
