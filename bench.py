@@ -434,7 +434,7 @@ def _row(ms, alg_bytes, traffic, peak, src):
 def bf16_rs_ag_leg(torch, rcc, dev_index, device, peak, src, K=10):
     """reduce_scatter then all_gather, 8 ranks x 2^26 bf16 per rank, N(0, 1)
     inputs, fp32 accumulation, rank-order sums; each collective timed alone
-    (median of K).  Minimum traffic (R + 1) * N * 2 bytes for both."""
+    (K launches back to back).  Minimum traffic (R + 1) * N * 2 bytes for both."""
     from gradient_sync_rcc_gb300 import synth
     R3, N3 = 8, 1 << 26
     n3 = N3 // R3
