@@ -487,3 +487,43 @@ def test_all_gather_list(orc, R, n):
             assert bits_equal(got, xs[q]), (r, q)
             if lists[r][q] is not None:
                 assert lists[r][q].guards_intact()
+
+
+@pytest.mark.parametrize("kind", ["reduce_scatter", "all_gather", "all_to_all"])
+@pytest.mark.parametrize("dtype", [rcc.F32, rcc.BF16])
+@pytest.mark.parametrize("out_off16", [True, False])
+def test_staged_kernels_on_16_byte_bases(orc, kind, dtype, out_off16):
+    """Odd shards whose buffers start 16 bytes past a 32-byte boundary: the
+    staged kernels' 16-byte-vector form, over many tiles plus head and tail,
+    bit for bit against the oracle, with the guard bands intact."""
+    R, n = 8, 65537
+    td = tdtype(dtype)
+    es = 4 if dtype == rcc.F32 else 2
+    off16 = 16 // es                               # elements in 16 bytes
+    kind_draw = "uniform" if dtype == rcc.F32 else "bf16_uniform"
+    out_off = off16 if out_off16 else 0
+    if kind == "all_gather":
+        xs = host_ranks(kind_draw, R, n, 1500, R, n)
+        ins = [Guarded(n, td, offset_elems=off16, fill=to_dev(x)) for x in xs]
+        outs = [Guarded(R * n, td, offset_elems=out_off) for _ in range(R)]
+        want = [np.concatenate(xs)] * R
+    else:
+        xs = host_ranks(kind_draw, R, R * n, 1501, R, n)
+        ins = [Guarded(R * n, td, offset_elems=off16, fill=to_dev(x)) for x in xs]
+        if kind == "reduce_scatter":
+            outs = [Guarded(n, td, offset_elems=out_off) for _ in range(R)]
+            want = orc.reduce_scatter(xs, "sum")
+        else:
+            outs = [Guarded(R * n, td, offset_elems=out_off) for _ in range(R)]
+            want = orc.all_to_all(xs)
+    with session(R, dtype, True) as h:
+        if kind == "reduce_scatter":
+            rcc.reduce_scatter(h, [g.t for g in ins], [o.t for o in outs], "sum")
+        elif kind == "all_gather":
+            rcc.all_gather(h, [g.t for g in ins], [o.t for o in outs])
+        else:
+            rcc.all_to_all_single(h, [g.t for g in ins], [o.t for o in outs])
+        torch.cuda.synchronize()
+    for r in range(R):
+        assert outs[r].guards_intact() and ins[r].guards_intact()
+        assert bits_equal(to_host(outs[r].t), want[r]), (kind, r)
