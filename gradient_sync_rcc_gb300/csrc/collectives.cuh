@@ -793,14 +793,6 @@ cudaError_t launch_w(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   return launch_kernel(fn, dim3(gx, (unsigned)nseg), dim3(kThreads), 0, stream, a);
 }
 
-// A runtime source count (NS == 0, more than 8 ranks) always takes 16-byte
-// vectors: with 32-byte ones its 8-source groups need about 100 registers (2
-// CTAs per SM), and at 9-64 ranks reduce and reduce_scatter measured 0.88-1.01
-// of the copy peak against 0.91-1.10 with 16-byte vectors (all_reduce alike).
-// 9-12 sources load as one group of 12 (one load round trip instead of two:
-// reduce and reduce_scatter at 9 ranks 0.93 / 0.91 -> 1.01 / 1.01); other
-// counts in groups of 8 (a group of 12 or 16 holds too many registers for
-// the occupancy that 16 ranks and up want: 1.09 -> 0.98 at 16).
 // A launch with more than one vector per thread (copies, and reductions over
 // one or two sources) takes half as many when its default grid stays below
 // the wave cap: twice the CTAs, so the last partial wave is half as long.  At
@@ -822,6 +814,14 @@ cudaError_t launch_unrolled_w(int nseg, const MultiPtrArgs& a, cudaStream_t stre
   return launch_w<T, NS, RED, FAST, W>(nseg, a, stream);
 }
 
+// A runtime source count (NS == 0, more than 8 ranks) always takes 16-byte
+// vectors: with 32-byte ones its 8-source groups need about 100 registers (2
+// CTAs per SM), and at 9-64 ranks reduce and reduce_scatter measured 0.88-1.01
+// of the copy peak against 0.91-1.10 with 16-byte vectors (all_reduce alike).
+// 9-12 sources load as one group of 12 (one load round trip instead of two:
+// reduce and reduce_scatter at 9 ranks 0.93 / 0.91 -> 1.01 / 1.01); other
+// counts in groups of 8 (a group of 12 or 16 holds too many registers for
+// the occupancy that 16 ranks and up want: 1.09 -> 0.98 at 16).
 template <typename T, int NS, int RED, bool FAST>
 cudaError_t launch_ns(int nseg, const MultiPtrArgs& a, cudaStream_t stream) {
   if constexpr (NS > 0) {
