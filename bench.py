@@ -83,7 +83,7 @@ def parse_args():
     ap.add_argument("--case", default="step",
                     choices=["step", "all_reduce", "reduce", "broadcast", "reduce_scatter",
                              "all_gather", "all_to_all", "grad_sync", "grad_sync_1024",
-                             "all_reduce_rank"],
+                             "all_reduce_rank", "checkpoint"],
                     help="step: the whole hot path (the benchmark line); otherwise time one "
                          "collective alone on --ranks x --elems (profiling and sweeps)")
     ap.add_argument("--ranks", type=int, default=R)
@@ -1103,6 +1103,64 @@ def bench_rank_case(args):
                       "min_traffic_bytes": traffic}), flush=True)
 
 
+def bench_checkpoint(args):
+    """Checkpoint save and restore of the 1,024-tensor optimizer state (4
+    ranks, `--replicas` state copies) after one grad-sync step:
+    checkpoint.state_dict copies params, exp_avg and exp_avg_sq to host
+    arrays; load_state_dict copies them back into the device tensors.  Both
+    are timed on the wall clock (each ends synchronised); the restored state
+    is compared bit for bit with what was saved."""
+    import torch
+    from gradient_sync_rcc_gb300 import build, checkpoint, rcc, synth
+    build.build()
+    dev = "cuda:0"
+    Rk, P, rep = 4, 1024, args.replicas
+    sizes = synth.param_sizes(P, 1024, 4194304, 20)
+    E = sum(sizes)
+    tensors = []
+    for i, n in enumerate(sizes):
+        g = [synth.gpu_draw("normal:1e-3", n, torch.float32, (22, i, 1, r), dev) * 65536.0
+             for r in range(Rk)]
+        p0 = synth.gpu_draw("normal:0.02", n, torch.float32, (21, i), dev)
+        tensors.append(dict(grads=g, params=[p0.clone() for _ in range(rep)],
+                            exp_avg=[torch.zeros(n, device=dev) for _ in range(rep)],
+                            exp_avg_sq=[torch.zeros(n, device=dev) for _ in range(rep)],
+                            mean_grad=torch.empty(n, device=dev)))
+    sets = rcc.ParamSets(tensors)
+    cfg = rcc.adamw_cfg(replicas=rep)
+    state = rcc.optim_state(scale=65536.0)
+    h = rcc.register(0, Rk, rcc.F32, True)
+    try:
+        rcc.grad_sync_adamw(h, sets, cfg, state)
+        torch.cuda.synchronize()
+    finally:
+        rcc.finish(h)
+    nbytes = 3 * 4 * E * rep
+    t0 = time.perf_counter()
+    sd = checkpoint.state_dict(tensors, cfg, state)
+    save_s = time.perf_counter() - t0
+    for t in tensors:
+        for k in ("params", "exp_avg", "exp_avg_sq"):
+            for x in t[k]:
+                x.zero_()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    checkpoint.load_state_dict(sd, tensors, rcc)
+    torch.cuda.synchronize()
+    load_s = time.perf_counter() - t0
+    same = all(np.array_equal(x.cpu().numpy(), sd["tensors"][i][k][j])
+               for i, t in enumerate(tensors) for k in ("params", "exp_avg", "exp_avg_sq")
+               for j, x in enumerate(t[k]))
+    print(json.dumps({"case": "checkpoint", "ranks": Rk, "tensors": P, "elements": E,
+                      "replicas": rep, "state_bytes": nbytes,
+                      "save_s": round(save_s, 3), "save_gbs": round(nbytes / save_s / 1e9, 2),
+                      "restore_s": round(load_s, 3),
+                      "restore_gbs": round(nbytes / load_s / 1e9, 2),
+                      "restored_bitwise": bool(same),
+                      "timing": "wall clock around each call, each ending synchronised"}),
+          flush=True)
+
+
 def bench_sweep(args):
     """The size sweep of the collectives (one process; each point the mean of
     back-to-back launches between one CUDA-event pair)."""
@@ -1157,6 +1215,9 @@ def main():
         return
     if args.case == "all_reduce_rank":
         bench_rank_case(args)
+        return
+    if args.case == "checkpoint":
+        bench_checkpoint(args)
         return
     if args.case != "step":
         bench_case(args)

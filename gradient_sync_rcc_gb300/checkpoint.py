@@ -19,14 +19,20 @@ import numpy as np
 STEP_OPTIONS_VERSION = 2
 
 
+def _host_copy(x):
+    """A host array that does not alias x: `.cpu()` of a device tensor is
+    already a fresh host copy; of a host tensor it is the tensor itself."""
+    a = x.detach().cpu().numpy()
+    return a if x.is_cuda else a.copy()
+
+
 def state_dict(tensors, cfg, state, fused_step=True):
     """Host copy of the optimizer state.  tensors: the dicts given to
     rcc.ParamSets (params / exp_avg / exp_avg_sq replica lists of device
     tensors); cfg: rcc.AdamWCfg; state: rcc.OptimState."""
     per = []
     for t in tensors:
-        per.append({k: [x.detach().cpu().numpy().copy() for x in t[k]]
-                    for k in ("params", "exp_avg", "exp_avg_sq")})
+        per.append({k: [_host_copy(x) for x in t[k]] for k in ("params", "exp_avg", "exp_avg_sq")})
     return {
         "tensors": per,
         "step": int(state.step),
