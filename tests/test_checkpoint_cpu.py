@@ -58,3 +58,20 @@ def test_step_options_checks():
     sd["step_options"].update(version=2, fused_step=False)
     with pytest.raises(ValueError):          # clipping requires the fused step
         checkpoint.step_options(sd)
+
+
+def test_state_dict_does_not_alias_host_tensors():
+    """A state taken from host tensors is a copy: changing the tensors after
+    state_dict leaves the saved arrays as they were."""
+    ts = _tensors()
+    cfg = rcc.adamw_cfg(replicas=2)
+    sd = checkpoint.state_dict(ts, cfg, rcc.optim_state())
+    before = [{k: [a.copy() for a in v] for k, v in t.items()} for t in sd["tensors"]]
+    for t in ts:
+        for k in t:
+            for x in t[k]:
+                x.add_(1.0)
+    for saved, ref in zip(sd["tensors"], before):
+        for k in ref:
+            for a, b in zip(saved[k], ref[k]):
+                assert np.array_equal(a, b)
